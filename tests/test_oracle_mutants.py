@@ -1,0 +1,121 @@
+"""Plant plausible mistakes in the oracle (on the CPU) and check that at least
+one pin in test_oracle_pins.py fails for each: evidence that the pins would
+catch a dropped term, a wrong sign or index, or a transposed operand."""
+
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import oracle.locks_oracle as L
+import tests.test_oracle_pins as pins
+
+
+def _lse_no_shift(x, axis=-1):
+    x = np.asarray(x, dtype=np.float64)
+    if x.shape[axis] == 0:
+        return np.full(np.delete(x.shape, axis if axis >= 0 else x.ndim + axis), -np.inf)
+    with np.errstate(over="ignore", divide="ignore"):
+        return np.log(np.sum(np.exp(x), axis=axis))
+
+
+def _logits_no_scale(q, V, C, mu=None, scale=None):
+    out = C @ (V.T @ np.asarray(q, dtype=np.float64))
+    if mu is not None:
+        out = out + float(np.asarray(q) @ mu)
+    return out
+
+
+def _logits_minus_mu(q, V, C, mu=None, scale=None):
+    d = np.asarray(q).shape[-1]
+    out = C @ (V.T @ np.asarray(q, dtype=np.float64))
+    if mu is not None:
+        out = out - float(np.asarray(q) @ mu)
+    return out / math.sqrt(d)
+
+
+def _gsa_raw_mean(shat):
+    shat = np.asarray(shat, dtype=np.float64)
+    return np.log(np.exp(shat).mean(axis=0))
+
+
+def _gsa_max(shat):
+    return np.max(np.asarray(shat, dtype=np.float64), axis=0)
+
+
+def _topk_ties_high(sigma, k):
+    sigma = np.asarray(sigma, dtype=np.float64)
+    n = sigma.size
+    k = max(0, min(int(k), n))
+    order = sorted(range(n), key=lambda j: (-sigma[j], -j))
+    return np.array(sorted(order[:k]), dtype=np.int64)
+
+
+def _summary_no_sigma(K, r, centered=False):
+    V, C, mu, S = ORIG["page_summary"](K, r, centered)
+    nz = np.linalg.norm(C, axis=0) > 0
+    C = C.copy()
+    C[:, nz] /= np.linalg.norm(C[:, nz], axis=0)
+    return V, C, mu, S
+
+
+def _summary_smallest(K, r, centered=False):
+    K = np.asarray(K, dtype=np.float64)
+    P, d = K.shape
+    mu = K.mean(axis=0) if centered else np.zeros(d)
+    U, S, Wt = np.linalg.svd(K - mu, full_matrices=False)
+    idx = np.argsort(S)[:r]
+    V = np.zeros((d, r))
+    C = np.zeros((P, r))
+    for c, i in enumerate(idx):
+        V[:, c] = Wt[i]
+        C[:, c] = U[:, i] * S[i]
+    return V, C, mu, S
+
+
+def _attention_no_scale(q, K, V, scale=None):
+    return ORIG["attention"](q, K, V, 1.0)
+
+
+ORIG = {n: getattr(L, n) for n in ("page_summary", "attention")}
+
+MUTANTS = {
+    "lse_without_max_shift": ("logsumexp", _lse_no_shift),
+    "logits_without_1_over_sqrt_d": ("reconstructed_logits", _logits_no_scale),
+    "centroid_term_sign": ("reconstructed_logits", _logits_minus_mu),
+    "gsa_raw_mass_mean": ("gsa_scores", _gsa_raw_mean),
+    "gsa_max_instead_of_mean": ("gsa_scores", _gsa_max),
+    "topk_ties_to_higher_index": ("select_top_pages", _topk_ties_high),
+    "summary_coefficients_without_sigma": ("page_summary", _summary_no_sigma),
+    "summary_smallest_singular_vectors": ("page_summary", _summary_smallest),
+    "attention_without_scale": ("attention", _attention_no_scale),
+}
+
+PIN_TESTS = [
+    pins.test_lse_brute_force_tiny_pages,
+    pins.test_scale_closed_form_ln10,
+    pins.test_summary_exact_low_rank_and_truncation,
+    pins.test_eckart_young_residual_optimal,
+    pins.test_centered_summary_identical_keys_closed_form,
+    pins.test_gsa_closed_form,
+    pins.test_gsa_normalisation_changes_ranking,
+    pins.test_topk_ties_go_to_lower_index_and_sorted,
+    pins.test_attention_closed_form_weights,
+    pins.test_summary_transpose_slip_detected,
+]
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, monkeypatch):
+    attr, fn = MUTANTS[name]
+    monkeypatch.setattr(L, attr, fn)
+    monkeypatch.setattr(oracle, attr, fn)
+    failed = []
+    for t in PIN_TESTS:
+        try:
+            with np.errstate(all="ignore"):
+                t()
+        except (AssertionError, ValueError, FloatingPointError, IndexError):
+            failed.append(t.__name__)
+    assert failed, f"no pin caught mutant {name}"
