@@ -1,0 +1,493 @@
+"""Benchmark of the LOCKS decode step on one GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config llama128k]
+                    [--impl reference] [--no-cpu-baseline]
+
+One step = the whole hot path on one batch: summary scan of every summarised
+page, group-shared top-k selection, sparse attention over the selected pages
+plus the tail (locks_decode_step), replayed from a CUDA graph.  Inputs are
+seeded synthetic page-local low-rank caches shaped like the named workload;
+summaries are built by the library's own GPU builder before timing.  L2 is
+defeated by rotating R independent copies of the cache and summaries whose
+total is several times the 129 MB L2.  Prints ONE JSON line.
+
+The in-library dense paged decode is timed the same way for the speedup, the
+summary-scan kernel alone for the roofline, and the fp64 CPU oracle on a
+bounded sample for the CPU baseline (the only place, with --impl reference,
+where this file runs the oracle).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+os.environ.setdefault("OMP_NUM_THREADS", "1")
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+os.environ.setdefault("MKL_NUM_THREADS", "1")
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from synth import CONFIGS, make_config_case  # noqa: E402
+
+METRIC = "decode-step µs & effective HBM GB/s (select+attend) at 128K/1M ctx vs dense"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+P, D = 64, 128
+
+# DRAM traffic of one summary-scan launch per summarised page-head (bytes),
+# from an ncu capture of the scan kernel (profiles/scan_kernel_llama128k.md);
+# valid only while scan.cu is unchanged since that capture.
+SCAN_TRAFFIC_PER_PAGE_HEAD = None
+SCAN_TRAFFIC_SOURCE_SHA = None
+
+
+# ---------------------------------------------------------------------------
+# byte model (algorithmic bytes; the pages' figures in tests/golden pin it)
+# ---------------------------------------------------------------------------
+
+def summary_bytes_per_page_head(rank: int, page: int = P, d: int = D, bytes_per=2) -> int:
+    return (rank * d + page * rank) * bytes_per
+
+
+def step_bytes(batch, hkv, G, n_sum, k, tail_tokens, rank) -> dict:
+    """Algorithmic bytes of one decode step: every summary once, s_hat written
+    and read once, K+V of the selected pages and the tail once, q and o."""
+    summ = batch * hkv * n_sum * summary_bytes_per_page_head(rank)
+    shat = 2 * batch * hkv * n_sum * G * 4
+    sel = batch * hkv * (k * P + tail_tokens) * D * 2 * 2
+    qo = 2 * batch * hkv * G * D * 2
+    return dict(summaries=summ, shat=shat, selected_kv=sel, qo=qo, total=summ + shat + sel + qo)
+
+
+def dense_bytes(batch, hkv, G, tokens) -> int:
+    return batch * hkv * tokens * D * 2 * 2 + 2 * batch * hkv * G * D * 2
+
+
+def residency(rank: int, page: int = P, d: int = D, basis_bits=16, coef_bits=16, centroid_bits=0) -> float:
+    """Resident summary bytes as a fraction of the page's K+V bytes (bf16 cache)."""
+    summ = (rank * d * basis_bits + page * rank * coef_bits + d * centroid_bits) / 8
+    return summ / (2 * page * d * 2)
+
+
+def _scan_source_sha() -> str:
+    with open(os.path.join(ROOT, "sparse_kv_page_rank_gb300", "csrc", "scan.cu"), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def _peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"locks_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# reference arm / CPU baseline: the fp64 oracle on a bounded sample
+# ---------------------------------------------------------------------------
+
+def _oracle_sample(case, cfg, kv_heads, budget_seconds: float, steps: int | None = None,
+                   max_pages: int | None = None):
+    """Time the oracle's decode step (summaries precomputed, not timed) on a
+    sample of KV heads of sequence 0, optionally cut to its first
+    ``max_pages`` pages.  The time per (sequence, KV head) problem is scaled
+    by the page ratio (the oracle's cost is linear in the pages it scans) and
+    by the number of problems.  Returns (us per full step, detail)."""
+    import oracle as O
+    from synth.generator import LocksCase
+    r = cfg["rank"]
+    G = case.group
+    b = 0
+    nfull_all = case.n_full_pages(b)
+    nfull = nfull_all if max_pages is None else min(nfull_all, max_pages)
+    seq_sample = np.array([nfull * P if nfull < nfull_all else int(case.seq_lens[b])], dtype=np.int32)
+    n_pages = -(-int(seq_sample[0]) // P)
+    phys = case.block_table[b, :n_pages]
+    bt = np.arange(n_pages, dtype=np.int32)[None, :]
+    subs = []
+    for h in kv_heads:
+        # one-sequence, one-KV-head slice of the cache on a compact pool, same bf16 inputs
+        kp = np.ascontiguousarray(case.k_pool[phys, h:h + 1])
+        vp = np.ascontiguousarray(case.v_pool[phys, h:h + 1])
+        sub = LocksCase(batch=1, num_q_heads=G, num_kv_heads=1, head_dim=D, page_size=P,
+                        seq_lens=seq_sample, block_table=bt, k_pool=kp, v_pool=vp,
+                        q=case.q[b:b + 1, h * G:(h + 1) * G], carriers=case.carriers[b:b + 1, h:h + 1],
+                        carrier_heads=case.carrier_heads[b:b + 1, h:h + 1],
+                        outlier_channels=case.outlier_channels, seed=case.seed)
+        basis = np.zeros((n_pages, 1, D, r))
+        coeffs = np.zeros((n_pages, 1, P, r))
+        for j in range(nfull):
+            V, C, _, _ = O.page_summary(O.bf16_widen(kp[j, 0]), r)
+            basis[j, 0], coeffs[j, 0] = V, C
+        subs.append((sub, basis, coeffs))
+    times = []
+    t_end = time.perf_counter() + budget_seconds
+    i = 0
+    while True:
+        sub, basis, coeffs = subs[i % len(subs)]
+        t0 = time.perf_counter()
+        O.decode_step(sub.q, sub.k_pool, sub.v_pool, sub.block_table, sub.seq_lens, [nfull], basis, coeffs,
+                      1, cfg["budget_tokens"])
+        times.append(time.perf_counter() - t0)
+        i += 1
+        if steps is not None:
+            if i >= steps:
+                break
+        elif time.perf_counter() > t_end and i >= len(subs):
+            break
+    per_problem = statistics.median(times) * (nfull_all / max(nfull, 1))
+    full = per_problem * case.batch * case.num_kv_heads
+    return full * 1e6, dict(problems_timed=i, per_problem_s=per_problem, times=times, pages=nfull,
+                            pages_full=nfull_all)
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    case, cfg = make_config_case(args.config)
+    W, K = args.warmup, args.steps
+    # each step: one (sequence, KV head) problem of the workload on a page
+    # window sized so that K + W steps take about two minutes, scaled to a full step
+    t0 = time.perf_counter()
+    _, probe = _oracle_sample(case, cfg, [0], 0.0, steps=1, max_pages=256)
+    per_page = probe["times"][0] / max(probe["pages"], 1)
+    window = int(max(16, min(case.n_full_pages(0), 120.0 / (K + W) / max(per_page, 1e-9))))
+    _oracle_sample(case, cfg, [0], 0.0, steps=max(W, 1), max_pages=window)
+    us_full, det = _oracle_sample(case, cfg, range(case.num_kv_heads), 0.0, steps=K, max_pages=window)
+    wall = time.perf_counter() - t0
+    line = {
+        "impl": "reference", "metric": METRIC, "value": us_full, "unit": "us", "n_gpus": args.gpus,
+        "steps": K, "warmup": W, "ms_per_step": us_full / 1e3, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": _config_dict(args.config, case, cfg),
+        "cpu_baseline": {"value": us_full, "unit": "us", "cores": 1, "kind": "oracle",
+                         "sample": f"each step = one (sequence, KV head) problem of {args.config} on its first "
+                                   f"{det['pages']} of {det['pages_full']} pages (summaries precomputed), "
+                                   f"median scaled by pages and x {case.batch * case.num_kv_heads} problems; "
+                                   f"{det['problems_timed']} steps, {wall:.1f} s"},
+        "e2e": {"value": us_full, "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def _config_dict(name, case, cfg, extra=None):
+    d = {"workload": f"{name}: batch {case.batch}, {case.num_q_heads} q heads / {case.num_kv_heads} kv heads, "
+                     f"head_dim {D}, page {P}, context {int(case.seq_lens[0])}, rank {cfg['rank']}, "
+                     f"budget {cfg['budget_tokens']} tokens, bf16",
+         "batch": case.batch, "num_q_heads": case.num_q_heads, "num_kv_heads": case.num_kv_heads,
+         "context": int(case.seq_lens[0]), "rank": cfg["rank"], "budget_tokens": cfg["budget_tokens"]}
+    if extra:
+        d.update(extra)
+    return d
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from sparse_kv_page_rank_gb300.build_lib import build
+    build()
+    from sparse_kv_page_rank_gb300 import locks as L
+    from sparse_kv_page_rank_gb300.runtime import LocksRuntime
+
+    case, cfg = make_config_case(args.config)
+    r, budget = cfg["rank"], cfg["budget_tokens"]
+    B, Hq, Hkv, G = case.batch, case.num_q_heads, case.num_kv_heads, case.group
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    k0, v0 = to_dev(case.k_pool), to_dev(case.v_pool)
+    bt = torch.from_numpy(case.block_table).to(dev)
+    sl = torch.from_numpy(case.seq_lens).to(dev)
+    nsum_host = np.array([case.n_full_pages(b) for b in range(B)], dtype=np.int32)
+    ns = torch.from_numpy(nsum_host).to(dev)
+    q = torch.from_numpy(case.q.view(np.int16)).view(torch.bfloat16).to(dev)
+    pages = torch.from_numpy(np.concatenate([case.block_table[b, :nsum_host[b]] for b in range(B)])).to(dev)
+
+    per_copy = k0.numel() * 4 + (r * D + P * r) * 2 * case.pages_total * Hkv
+    # bytes one step touches (summaries + selected pages); rotate enough copies
+    # that consecutive replays of the same copy are > 4x L2 apart
+    touched = Hkv * int(nsum_host.sum()) * summary_bytes_per_page_head(r) + \
+        B * Hkv * min(budget // P, case.max_pages) * P * D * 4
+    R = max(2, min(16, math.ceil(4 * 129e6 / max(touched, 1))))
+    rts = []
+    for i in range(R):
+        kk = k0 if i == 0 else k0.clone()
+        vv = v0 if i == 0 else v0.clone()
+        rt = LocksRuntime(kk, vv, bt, sl, ns, Hq, r, budget)
+        rts.append(rt)
+    del case.k_pool, case.v_pool
+    # summaries by the library's builder (timed once, outside the step)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    rts[0].build_summaries(pages)
+    e1.record()
+    torch.cuda.synchronize()
+    build_ms = e0.elapsed_time(e1)
+    build_pages_per_s = pages.numel() * Hkv / (build_ms / 1e3)
+    for rt in rts[1:]:
+        rt.set_summaries(rts[0].basis_t, rts[0].coeffs)
+    torch.cuda.synchronize()
+    assert rts[0].device_error() == 0
+
+    stream = torch.cuda.Stream(device=dev)
+    page_lse_bufs = [torch.empty((B, Hq, case.max_pages), dtype=torch.float32, device=dev) for _ in rts]
+
+    def capture(fn_per_rt):
+        graphs = []
+        for i, rt in enumerate(rts):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                fn_per_rt(i, rt)
+                with torch.cuda.graph(g, stream=stream):
+                    fn_per_rt(i, rt)
+            graphs.append(g)
+        torch.cuda.synchronize()
+        return graphs
+
+    step_graphs = capture(lambda i, rt: rt.decode_step(q, stream=stream))
+    dense_graphs = capture(lambda i, rt: rt.dense_decode(q, rt.out, rt.lse, stream=stream))
+    scan_graphs = capture(lambda i, rt: rt.page_scores(q, page_lse_bufs[i], stream=stream))
+
+    def timed(graphs, K, W):
+        with torch.cuda.stream(stream):
+            for i in range(W):
+                graphs[i % len(graphs)].replay()
+        stream.synchronize()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            s0.record(stream)
+            for i in range(K):
+                graphs[i % len(graphs)].replay()
+            s1.record(stream)
+        s1.synchronize()
+        torch.cuda.synchronize()
+        ms = s0.elapsed_time(s1)
+        if world > 1:
+            t = torch.tensor([ms], dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms / K
+
+    K, W = args.steps, max(3, args.warmup)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    step_ms = timed(step_graphs, K, W)
+    clk = clocks.stop()
+    dense_ms = timed(dense_graphs, max(20, K // 4), W)
+    scan_ms = timed(scan_graphs, K, W)
+
+    # e2e through the public API: pinned host q -> device, decode step, out -> pinned host
+    q_host = q.cpu().pin_memory()
+    out_host = torch.empty((B, Hq, D), dtype=torch.bfloat16).pin_memory()
+    q_dev = torch.empty_like(q)
+    e2e_graphs = []
+    for rt in rts:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            q_dev.copy_(q_host, non_blocking=True)
+            rt.decode_step(q_dev, stream=stream)
+            out_host.copy_(rt.out, non_blocking=True)
+            with torch.cuda.graph(g, stream=stream):
+                q_dev.copy_(q_host, non_blocking=True)
+                rt.decode_step(q_dev, stream=stream)
+                out_host.copy_(rt.out, non_blocking=True)
+        e2e_graphs.append(g)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    e2e_ms_dev = timed(e2e_graphs, K, W)
+    e2e_wall_ms = (time.perf_counter() - t0) * 1e3
+
+    # quality: mass recall of the selected pages against the exact page LSE
+    # (read-every-key, on the GPU), and carrier retention
+    rt = rts[0]
+    rt.decode_step(q)
+    exact = rt.exact_page_lse(q)
+    torch.cuda.synchronize()
+    sel = rt.sel_pages.cpu().numpy()
+    cnt = rt.sel_count.cpu().numpy()
+    ex = exact.double().cpu().numpy()
+    recalls, oracle_recalls, kept, total = [], [], 0, 0
+    for b in range(B):
+        n = int(nsum_host[b])
+        for h in range(Hkv):
+            k = int(cnt[b, h])
+            s_star = ex[b, h * G:(h + 1) * G, :n]
+            tot = np.logaddexp.reduce(s_star, axis=1)
+            chosen = sel[b, h, :cnt[b, h]]
+            part = np.logaddexp.reduce(s_star[:, chosen], axis=1)
+            recalls.append(float(np.mean(np.exp(part - tot))))
+            # exact-LSE selection (same GSA rule on s*): best achievable recall
+            z = s_star - tot[:, None]
+            sig = np.logaddexp.reduce(z, axis=0)
+            best = np.lexsort((np.arange(n), -sig))[:k]
+            oracle_recalls.append(float(np.mean(np.exp(np.logaddexp.reduce(s_star[:, best], axis=1) - tot))))
+            cs = set(chosen.tolist())
+            for cpg in case.carriers[b, h]:
+                if cpg >= 0:
+                    total += 1
+                    kept += int(cpg) in cs
+    assert rt.device_error() == 0
+
+    n_sum_tot = int(nsum_host.sum())
+    sb = dict(summaries=0, shat=0, selected_kv=0, qo=0, total=0)
+    for b in range(B):
+        bb = step_bytes(1, Hkv, G, int(nsum_host[b]), int(cnt[b].mean()),
+                        int(case.seq_lens[b]) - int(nsum_host[b]) * P, r)
+        for key in sb:
+            sb[key] += bb[key]
+    db = sum(dense_bytes(1, Hkv, G, int(case.seq_lens[b])) for b in range(B))
+    scan_alg = Hkv * n_sum_tot * (summary_bytes_per_page_head(r) + G * 4)
+    peak, peak_kind = _peaks()
+    step_us = step_ms * 1e3
+    eff_gbs = sb["total"] / (step_ms * 1e-3) / 1e9
+    scan_gbs = scan_alg / (scan_ms * 1e-3) / 1e9
+    dense_gbs = db / (dense_ms * 1e-3) / 1e9
+    traffic = None
+    if SCAN_TRAFFIC_PER_PAGE_HEAD is not None and SCAN_TRAFFIC_SOURCE_SHA == _scan_source_sha():
+        traffic = SCAN_TRAFFIC_PER_PAGE_HEAD * Hkv * n_sum_tot
+
+    # CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from synth import make_config_case as mk
+        case2, cfg2 = mk(args.config)
+        us_full, det = _oracle_sample(case2, cfg2, range(min(Hkv, 2)), args.cpu_seconds)
+        cpu = {"value": us_full, "unit": "us", "cores": 1, "kind": "oracle",
+               "sample": f"fp64 numpy oracle decode step (summaries precomputed) on KV heads 0-"
+                         f"{min(Hkv, 2) - 1} of sequence 0, {det['problems_timed']} problems in "
+                         f"~{args.cpu_seconds:.0f} s, median per problem x {B * Hkv} problems"}
+
+    line = {
+        "metric": METRIC, "value": step_us, "unit": "us", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": step_ms, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": _config_dict(args.config, case, cfg, {
+            "l2": f"rotating {R} independent copies of cache + summaries "
+                  f"({R * per_copy / 1e9:.2f} GB > 129 MB L2)",
+            "graph": "CUDA graph replay of locks_decode_step"}),
+        "effective_gbs": eff_gbs,
+        "step_frac_of_hbm": eff_gbs / peak,
+        "dense_us": dense_ms * 1e3, "dense_effective_gbs": dense_gbs, "speedup_vs_dense": dense_ms / step_ms,
+        "step_bytes": sb, "dense_bytes": db, "kv_bytes_ratio": db / sb["total"],
+        "residency": residency(r), "mass_recall": float(np.mean(recalls)),
+        "exact_lse_selection_recall": float(np.mean(oracle_recalls)),
+        "carrier_retention": kept / total if total else None,
+        "summary_build": {"pages_per_s": build_pages_per_s, "ms": build_ms, "page_heads": int(pages.numel() * Hkv)},
+        "roofline": {"kernel": "scan_kernel (summary scan)", "bound": "hbm", "achieved": scan_gbs,
+                     "peak": peak, "unit": "GB/s", "frac": scan_gbs / peak, "traffic": traffic,
+                     "peak_kind": f"{peak_kind} (hbm_gbs, burst copy)", "scan_us": scan_ms * 1e3,
+                     "algorithmic_bytes": scan_alg},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_ms_dev * 1e3, "unit": "us", "h2d_bytes_per_step": int(q.numel() * 2),
+                "d2h_bytes_per_step": int(B * Hq * D * 2),
+                "how": "CUDA graph: cudaMemcpyAsync pinned q -> device, locks_decode_step, out -> pinned host",
+                "host_wall_us_per_step": e2e_wall_ms * 1e3 / (K + W)},
+        "gpu_launches": 3 * K,
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", default="llama128k", choices=sorted(CONFIGS))
+    ap.add_argument("--impl", default="locks", choices=["locks", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,428 @@
+// C ABI of liblocks.so: host-side validation, launch planning, workspace
+// layout, TMA descriptor encoding and kernel launches.  Nothing here
+// allocates device memory or synchronises a stream (except
+// locks_get_device_error).
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/locks.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace {
+
+using namespace locks;
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+int device_sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 152;
+  if (dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+  if (dev < 64) cache[dev] = n;
+  return n;
+}
+
+struct Plan {
+  int G = 0, Hq = 0, BH = 0, k_max = 0;
+  int scan_chunk = 0, n_scan = 0;
+  int tk_chunk = 0, n_tk = 0;
+  size_t tk_keys = 0;
+  int sparse_splits = 0, dense_splits = 0, max_splits = 0;
+  size_t off_err = 0, off_cnt_tk = 0, off_cnt_att = 0, off_shat = 0, off_part = 0, off_ckey = 0,
+         off_cidx = 0, off_ccnt = 0, off_sel = 0, off_selcnt = 0, off_pml = 0, off_po = 0, total = 0;
+};
+
+locks_status_t check_cache(const locks_cache_t* c, bool need_kv) {
+  if (!c) return LOCKS_ERR_INVALID_ARG;
+  if (c->batch <= 0 || c->num_kv_heads <= 0 || c->pages_total <= 0 || c->max_pages <= 0)
+    return LOCKS_ERR_INVALID_ARG;
+  if (c->head_dim != kHeadDim || c->page_size != kPage) return LOCKS_ERR_UNSUPPORTED;
+  if (need_kv) {
+    if (!c->k_pool || !c->v_pool || !c->block_table || !c->seq_lens) return LOCKS_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(c->k_pool) | reinterpret_cast<uintptr_t>(c->v_pool)) & 15)
+      return LOCKS_ERR_INVALID_ARG;
+  }
+  // TMA row coordinate and 32-bit page-head offsets
+  if ((long long)c->pages_total * c->num_kv_heads * kPage > 0x7fffffffLL) return LOCKS_ERR_UNSUPPORTED;
+  if ((long long)c->max_pages * kPage > 0x7fffffffLL) return LOCKS_ERR_UNSUPPORTED;
+  return LOCKS_OK;
+}
+
+locks_status_t check_params(const locks_cache_t* c, const locks_params_t* p) {
+  if (!p) return LOCKS_ERR_INVALID_ARG;
+  if (p->num_q_heads <= 0 || p->num_q_heads % c->num_kv_heads) return LOCKS_ERR_INVALID_ARG;
+  const int G = p->num_q_heads / c->num_kv_heads;
+  if (G > 16) return LOCKS_ERR_UNSUPPORTED;
+  if (p->budget_tokens < 0 || p->flags != 0) return LOCKS_ERR_INVALID_ARG;
+  if (!(p->scale >= 0.f) || !std::isfinite(p->scale)) return LOCKS_ERR_INVALID_ARG;
+  return LOCKS_OK;
+}
+
+locks_status_t check_summary(const locks_summary_t* s, bool for_scan) {
+  if (!s || !s->basis_t || !s->coeffs) return LOCKS_ERR_INVALID_ARG;
+  if (s->rank < 2 || s->rank > 16 || (s->rank & 1)) return LOCKS_ERR_UNSUPPORTED;
+  if (s->dtype != LOCKS_DTYPE_BF16 && s->dtype != LOCKS_DTYPE_F32) return LOCKS_ERR_INVALID_ARG;
+  if (for_scan && s->dtype != LOCKS_DTYPE_BF16) return LOCKS_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(s->basis_t) | reinterpret_cast<uintptr_t>(s->coeffs)) & 15)
+    return LOCKS_ERR_INVALID_ARG;
+  return LOCKS_OK;
+}
+
+float scale_of(const locks_params_t* p) {
+  return p->scale > 0.f ? p->scale : 1.0f / std::sqrt((float)kHeadDim);
+}
+
+Plan make_plan(const locks_cache_t* c, const locks_params_t* p) {
+  Plan pl;
+  const int sms = device_sm_count();
+  pl.G = p->num_q_heads / c->num_kv_heads;
+  pl.Hq = p->num_q_heads;
+  pl.BH = c->batch * c->num_kv_heads;
+  pl.k_max = std::min(p->budget_tokens / kPage, c->max_pages);
+  const long long BH = pl.BH;
+
+  // scan: about two resident CTAs per SM, pages per CTA a multiple of the warp count
+  {
+    const long long target = 2LL * sms;
+    long long per = (BH * c->max_pages + target - 1) / target;
+    per = std::max<long long>(kScanWarps, (per + kScanWarps - 1) / kScanWarps * kScanWarps);
+    pl.scan_chunk = (int)std::min<long long>(per, (long long)c->max_pages + kScanWarps);
+    pl.n_scan = (c->max_pages + pl.scan_chunk - 1) / pl.scan_chunk;
+  }
+  // top-k: chunks of 1024 pages; grow chunks while candidates would overflow
+  {
+    int chunk = 1024;
+    int n = (c->max_pages + chunk - 1) / chunk;
+    while (n > 1 && (long long)n * std::max(pl.k_max, 1) > 16384 && chunk < 16384) {
+      chunk *= 2;
+      n = (c->max_pages + chunk - 1) / chunk;
+    }
+    pl.tk_chunk = chunk;
+    pl.n_tk = n;
+    pl.tk_keys = std::max<size_t>((size_t)std::min(chunk, c->max_pages), (size_t)n * std::max(pl.k_max, 1));
+  }
+  // attention: about three resident CTAs per SM
+  {
+    const long long target = 3LL * sms;
+    const long long items = (long long)pl.k_max + 2;
+    if (BH * items <= target)
+      pl.sparse_splits = (int)items;
+    else
+      pl.sparse_splits = (int)std::max<long long>(1, target / BH);
+    pl.sparse_splits = std::max(1, std::min<int>(pl.sparse_splits, (int)items));
+    long long ds = (target + BH - 1) / BH;
+    pl.dense_splits = (int)std::max<long long>(1, std::min<long long>(ds, c->max_pages));
+    pl.max_splits = std::max(pl.sparse_splits, pl.dense_splits);
+  }
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + std::max<size_t>(bytes, 1));
+    return o;
+  };
+  pl.off_err = take(sizeof(int));
+  pl.off_cnt_tk = take(sizeof(unsigned) * BH);
+  pl.off_cnt_att = take(sizeof(unsigned) * BH);
+  pl.off_shat = take(sizeof(float) * BH * c->max_pages * pl.G);
+  pl.off_part = take(sizeof(float2) * BH * pl.n_scan * pl.G);
+  pl.off_ckey = take(sizeof(uint32_t) * BH * pl.n_tk * std::max(pl.k_max, 1));
+  pl.off_cidx = take(sizeof(int32_t) * BH * pl.n_tk * std::max(pl.k_max, 1));
+  pl.off_ccnt = take(sizeof(int32_t) * BH * pl.n_tk);
+  pl.off_sel = take(sizeof(int32_t) * BH * std::max(pl.k_max, 1));
+  pl.off_selcnt = take(sizeof(int32_t) * BH);
+  pl.off_pml = take(sizeof(float2) * BH * pl.max_splits * pl.G);
+  pl.off_po = take(sizeof(float) * BH * pl.max_splits * pl.G * kHeadDim);
+  pl.total = off;
+  return pl;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+locks_status_t check_ws(void* ws, size_t bytes, const Plan& pl) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) || bytes < pl.total) return LOCKS_ERR_WORKSPACE;
+  return LOCKS_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D view of a pool: rows = pages_total * Hkv * P tokens, 128 bf16 columns;
+// 64 x 64 boxes with 128-byte swizzle.
+bool encode_pool(CUtensorMap* m, const void* pool, const locks_cache_t* c) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)c->pages_total * c->num_kv_heads * kPage};
+  cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
+  cuuint32_t box[2] = {64, 64};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+locks_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? LOCKS_OK : LOCKS_ERR_CUDA; }
+
+locks_status_t run_select(const locks_cache_t* c, const locks_summary_t* s, const locks_params_t* p,
+                          const Plan& pl, const void* q, int32_t* sel, int32_t* selcnt, float* page_lse,
+                          void* ws, cudaStream_t st) {
+  ScanArgs sa;
+  sa.basis_t = static_cast<const uint16_t*>(s->basis_t);
+  sa.coeffs = static_cast<const uint16_t*>(s->coeffs);
+  sa.q = static_cast<const uint16_t*>(q);
+  sa.block_table = c->block_table;
+  sa.seq_lens = c->seq_lens;
+  sa.n_summarized = c->n_summarized;
+  sa.shat = at<float>(ws, pl.off_shat);
+  sa.part = at<float2>(ws, pl.off_part);
+  sa.page_lse = page_lse;
+  sa.err = at<int>(ws, pl.off_err);
+  sa.batch = c->batch;
+  sa.num_kv_heads = c->num_kv_heads;
+  sa.group = pl.G;
+  sa.rank = s->rank;
+  sa.max_pages = c->max_pages;
+  sa.pages_total = c->pages_total;
+  sa.chunk_pages = pl.scan_chunk;
+  sa.n_chunks = pl.n_scan;
+  sa.scale_log2 = scale_of(p) * kLog2e;
+  cudaError_t e = launch_scan(sa, st, true);
+  if (e != cudaSuccess) return LOCKS_ERR_CUDA;
+  if (!sel) return LOCKS_OK;  // scan only
+
+  TopkArgs ta;
+  ta.shat = sa.shat;
+  ta.part = sa.part;
+  ta.n_scan_chunks = pl.n_scan;
+  ta.seq_lens = c->seq_lens;
+  ta.n_summarized = c->n_summarized;
+  ta.cand_key = at<uint32_t>(ws, pl.off_ckey);
+  ta.cand_idx = at<int32_t>(ws, pl.off_cidx);
+  ta.cand_cnt = at<int32_t>(ws, pl.off_ccnt);
+  ta.counters = at<unsigned>(ws, pl.off_cnt_tk);
+  ta.sel_pages = sel;
+  ta.sel_count = selcnt;
+  ta.err = sa.err;
+  ta.batch = c->batch;
+  ta.num_kv_heads = c->num_kv_heads;
+  ta.group = pl.G;
+  ta.max_pages = c->max_pages;
+  ta.k_max = pl.k_max;
+  ta.chunk_pages = pl.tk_chunk;
+  ta.n_chunks = pl.n_tk;
+  ta.smem_keys = pl.tk_keys;
+  return cuda_status(launch_topk(ta, st, true));
+}
+
+locks_status_t run_attend(const locks_cache_t* c, const locks_params_t* p, const Plan& pl, const void* q,
+                          const int32_t* sel, const int32_t* selcnt, void* out, float* lse, float* page_lse,
+                          void* ws, int mode, cudaStream_t st) {
+  CUtensorMap tk, tv;
+  std::memset(&tk, 0, sizeof(tk));
+  std::memset(&tv, 0, sizeof(tv));
+  if (!encode_pool(&tk, c->k_pool, c)) return LOCKS_ERR_CUDA;
+  if (mode != kAttendPageLse && !encode_pool(&tv, c->v_pool, c)) return LOCKS_ERR_CUDA;
+  AttendArgs a;
+  a.q = static_cast<const uint16_t*>(q);
+  a.block_table = c->block_table;
+  a.seq_lens = c->seq_lens;
+  a.n_summarized = c->n_summarized;
+  a.sel_pages = sel;
+  a.sel_count = selcnt;
+  a.out = static_cast<uint16_t*>(out);
+  a.lse = lse;
+  a.page_lse = page_lse;
+  a.part_o = ws ? at<float>(ws, pl.off_po) : nullptr;
+  a.part_ml = ws ? at<float2>(ws, pl.off_pml) : nullptr;
+  a.counters = ws ? at<unsigned>(ws, pl.off_cnt_att) : nullptr;
+  a.err = ws ? at<int>(ws, pl.off_err) : nullptr;
+  a.batch = c->batch;
+  a.num_kv_heads = c->num_kv_heads;
+  a.group = pl.G;
+  a.max_pages = c->max_pages;
+  a.pages_total = c->pages_total;
+  a.k_max = pl.k_max;
+  a.n_splits = mode == kAttendSparse ? pl.sparse_splits : pl.dense_splits;
+  a.scale_log2 = scale_of(p) * kLog2e;
+  return cuda_status(launch_attend(a, tk, tv, mode, st, true));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* locks_status_string(locks_status_t s) {
+  switch (s) {
+    case LOCKS_OK: return "LOCKS_OK";
+    case LOCKS_ERR_INVALID_ARG: return "LOCKS_ERR_INVALID_ARG";
+    case LOCKS_ERR_UNSUPPORTED: return "LOCKS_ERR_UNSUPPORTED";
+    case LOCKS_ERR_CUDA: return "LOCKS_ERR_CUDA";
+    case LOCKS_ERR_WORKSPACE: return "LOCKS_ERR_WORKSPACE";
+    case LOCKS_ERR_DEVICE: return "LOCKS_ERR_DEVICE";
+  }
+  return "LOCKS_ERR_UNKNOWN";
+}
+
+locks_status_t locks_workspace_size(const locks_cache_t* cache, const locks_summary_t* summary,
+                                    const locks_params_t* params, size_t* bytes) {
+  (void)summary;
+  if (!bytes) return LOCKS_ERR_INVALID_ARG;
+  locks_status_t st = check_cache(cache, false);
+  if (st != LOCKS_OK) return st;
+  if ((st = check_params(cache, params)) != LOCKS_OK) return st;
+  *bytes = make_plan(cache, params).total;
+  return LOCKS_OK;
+}
+
+locks_status_t locks_workspace_init(void* ws, size_t bytes, void* stream) {
+  if (!ws) return LOCKS_ERR_INVALID_ARG;
+  return cuda_status(cudaMemsetAsync(ws, 0, bytes, static_cast<cudaStream_t>(stream)));
+}
+
+locks_status_t locks_build_summaries(const locks_cache_t* cache, locks_summary_t* summary,
+                                     const int32_t* page_ids, int32_t n, void* ws, size_t ws_bytes,
+                                     void* stream) {
+  if (!cache || !cache->k_pool) return LOCKS_ERR_INVALID_ARG;
+  locks_status_t st = check_cache(cache, false);
+  if (st != LOCKS_OK) return st;
+  if ((st = check_summary(summary, false)) != LOCKS_OK) return st;
+  if (n < 0 || (n > 0 && !page_ids)) return LOCKS_ERR_INVALID_ARG;
+  if ((long long)n * cache->num_kv_heads > 0x7fffffffLL) return LOCKS_ERR_INVALID_ARG;
+  if (ws && (ws_bytes < sizeof(int) || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1))))
+    return LOCKS_ERR_WORKSPACE;
+  BuildArgs a;
+  a.k_pool = static_cast<const uint16_t*>(cache->k_pool);
+  a.basis_t = summary->basis_t;
+  a.coeffs = summary->coeffs;
+  a.page_ids = page_ids;
+  a.n = n;
+  a.num_kv_heads = cache->num_kv_heads;
+  a.rank = summary->rank;
+  a.pages_total = cache->pages_total;
+  a.out_f32 = summary->dtype == LOCKS_DTYPE_F32;
+  a.err = ws ? static_cast<int*>(ws) : nullptr;  // the error word is at offset 0 of every workspace
+  return cuda_status(launch_build(a, static_cast<cudaStream_t>(stream)));
+}
+
+locks_status_t locks_select(const locks_cache_t* cache, const locks_summary_t* summary,
+                            const locks_params_t* params, const void* q, int32_t* sel_pages,
+                            int32_t* sel_count, float* page_lse, void* ws, size_t ws_bytes, void* stream) {
+  locks_status_t st = check_cache(cache, false);
+  if (st != LOCKS_OK) return st;
+  if (!cache->block_table || !cache->seq_lens || !cache->n_summarized) return LOCKS_ERR_INVALID_ARG;
+  if ((st = check_params(cache, params)) != LOCKS_OK) return st;
+  if ((st = check_summary(summary, true)) != LOCKS_OK) return st;
+  if (!q || !sel_pages || !sel_count) return LOCKS_ERR_INVALID_ARG;
+  Plan pl = make_plan(cache, params);
+  if ((st = check_ws(ws, ws_bytes, pl)) != LOCKS_OK) return st;
+  return run_select(cache, summary, params, pl, q, sel_pages, sel_count, page_lse, ws,
+                    static_cast<cudaStream_t>(stream));
+}
+
+locks_status_t locks_page_scores(const locks_cache_t* cache, const locks_summary_t* summary,
+                                 const locks_params_t* params, const void* q, float* page_lse, void* ws,
+                                 size_t ws_bytes, void* stream) {
+  locks_status_t st = check_cache(cache, false);
+  if (st != LOCKS_OK) return st;
+  if (!cache->block_table || !cache->seq_lens || !cache->n_summarized) return LOCKS_ERR_INVALID_ARG;
+  if ((st = check_params(cache, params)) != LOCKS_OK) return st;
+  if ((st = check_summary(summary, true)) != LOCKS_OK) return st;
+  if (!q || !page_lse) return LOCKS_ERR_INVALID_ARG;
+  Plan pl = make_plan(cache, params);
+  if ((st = check_ws(ws, ws_bytes, pl)) != LOCKS_OK) return st;
+  return run_select(cache, summary, params, pl, q, nullptr, nullptr, page_lse, ws,
+                    static_cast<cudaStream_t>(stream));
+}
+
+locks_status_t locks_sparse_attend(const locks_cache_t* cache, const locks_params_t* params, const void* q,
+                                   const int32_t* sel_pages, const int32_t* sel_count, void* out, float* lse,
+                                   void* ws, size_t ws_bytes, void* stream) {
+  locks_status_t st = check_cache(cache, true);
+  if (st != LOCKS_OK) return st;
+  if (!cache->n_summarized) return LOCKS_ERR_INVALID_ARG;
+  if ((st = check_params(cache, params)) != LOCKS_OK) return st;
+  if (!q || !sel_pages || !sel_count || !out) return LOCKS_ERR_INVALID_ARG;
+  Plan pl = make_plan(cache, params);
+  if ((st = check_ws(ws, ws_bytes, pl)) != LOCKS_OK) return st;
+  return run_attend(cache, params, pl, q, sel_pages, sel_count, out, lse, nullptr, ws, kAttendSparse,
+                    static_cast<cudaStream_t>(stream));
+}
+
+locks_status_t locks_decode_step(const locks_cache_t* cache, const locks_summary_t* summary,
+                                 const locks_params_t* params, const void* q, void* out, float* lse,
+                                 int32_t* sel_pages, int32_t* sel_count, void* ws, size_t ws_bytes,
+                                 void* stream) {
+  locks_status_t st = check_cache(cache, true);
+  if (st != LOCKS_OK) return st;
+  if (!cache->n_summarized) return LOCKS_ERR_INVALID_ARG;
+  if ((st = check_params(cache, params)) != LOCKS_OK) return st;
+  if ((st = check_summary(summary, true)) != LOCKS_OK) return st;
+  if (!q || !out || ((sel_pages == nullptr) != (sel_count == nullptr))) return LOCKS_ERR_INVALID_ARG;
+  Plan pl = make_plan(cache, params);
+  if ((st = check_ws(ws, ws_bytes, pl)) != LOCKS_OK) return st;
+  int32_t* sel = sel_pages ? sel_pages : at<int32_t>(ws, pl.off_sel);
+  int32_t* cnt = sel_count ? sel_count : at<int32_t>(ws, pl.off_selcnt);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((st = run_select(cache, summary, params, pl, q, sel, cnt, nullptr, ws, s)) != LOCKS_OK) return st;
+  return run_attend(cache, params, pl, q, sel, cnt, out, lse, nullptr, ws, kAttendSparse, s);
+}
+
+locks_status_t locks_dense_decode(const locks_cache_t* cache, const locks_params_t* params, const void* q,
+                                  void* out, float* lse, void* ws, size_t ws_bytes, void* stream) {
+  locks_status_t st = check_cache(cache, true);
+  if (st != LOCKS_OK) return st;
+  if ((st = check_params(cache, params)) != LOCKS_OK) return st;
+  if (!q || !out) return LOCKS_ERR_INVALID_ARG;
+  Plan pl = make_plan(cache, params);
+  if ((st = check_ws(ws, ws_bytes, pl)) != LOCKS_OK) return st;
+  return run_attend(cache, params, pl, q, nullptr, nullptr, out, lse, nullptr, ws, kAttendDense,
+                    static_cast<cudaStream_t>(stream));
+}
+
+locks_status_t locks_exact_page_lse(const locks_cache_t* cache, const locks_params_t* params, const void* q,
+                                    float* page_lse, void* stream) {
+  if (!cache || !cache->k_pool || !cache->block_table || !cache->seq_lens) return LOCKS_ERR_INVALID_ARG;
+  locks_status_t st = check_cache(cache, false);
+  if (st != LOCKS_OK) return st;
+  if ((reinterpret_cast<uintptr_t>(cache->k_pool) & 15)) return LOCKS_ERR_INVALID_ARG;
+  if ((st = check_params(cache, params)) != LOCKS_OK) return st;
+  if (!q || !page_lse) return LOCKS_ERR_INVALID_ARG;
+  Plan pl = make_plan(cache, params);
+  return run_attend(cache, params, pl, q, nullptr, nullptr, nullptr, nullptr, page_lse, nullptr, kAttendPageLse,
+                    static_cast<cudaStream_t>(stream));
+}
+
+locks_status_t locks_get_device_error(void* ws, int32_t* code, void* stream) {
+  if (!ws || !code) return LOCKS_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int v = 0;
+  if (cudaMemcpyAsync(&v, ws, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return LOCKS_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return LOCKS_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, sizeof(int), s) != cudaSuccess) return LOCKS_ERR_CUDA;
+  *code = v;
+  return v ? LOCKS_ERR_DEVICE : LOCKS_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,415 @@
+// Paged flash-decode over a page list.
+//
+// Sparse mode: exact attention over the selected pages plus the open tail
+// (LOCKS abstract: "attends only the top pages"; blog "Ringkasan spektral per
+// halaman": only the top pages are processed).  Dense mode: every page of
+// every sequence (the in-library baseline).  Page-LSE mode: the exact
+// per-page log-sum-exp that reads every key (the "read-every-key exact-LSE
+// oracle" the abstract measures selection against).
+//
+// Work split: grid (n_splits, B*Hkv).  The page list of problem bh
+// (sel_pages[0..cnt) then the tail pages, or every page) is cut into n_splits
+// contiguous ranges.  A CTA of four warps streams its pages through a
+// two-stage shared-memory ring: one thread issues 2-D TMA loads
+// (cp.async.bulk.tensor, 64 x 64 bf16 boxes, 128-byte swizzle) of the page's
+// K and V tiles (16 KiB each) and an mbarrier with a transaction count tells
+// the warps when they have landed.  Warp w owns tokens 16w..16w+15 of every
+// page: S = Q K^T on tensor cores (m16n8k16, M = the G <= 16 query heads of
+// the group), an online base-2 softmax in registers, then O += P V with P
+// reused from the accumulator layout and V fragments read by ldmatrix.trans.
+// Partial results (max, sum, O) of the four warps are merged in shared memory;
+// the CTAs of one problem are merged by the last CTA to finish (atomic ticket,
+// no spinning), which writes o (bf16) and lse (natural log).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace locks {
+
+namespace {
+
+constexpr int kWarps = kAttendThreads / 32;
+constexpr int kHalfTile = 64 * 128;        // bytes of one 64-row x 64-col bf16 box
+constexpr int kTile = 2 * kHalfTile;       // one page-head of K (or V): 16 KiB
+constexpr int kStage = 2 * kTile;          // K + V
+constexpr int kStages = 2;
+constexpr int kOStride = 132;              // padded row of the O merge buffer (floats)
+
+__device__ __forceinline__ uint32_t tile_addr(uint32_t base, int row, int chunk16) {
+  // 128B swizzle: 16-byte chunk index XOR (row mod 8) within each 128-byte row
+  const int half = chunk16 >> 3, cc = chunk16 & 7;
+  return base + half * kHalfTile + row * 128 + ((cc ^ (row & 7)) << 4);
+}
+
+struct Item {
+  int lp;     // logical page, -1 = invalid
+  int phys;   // physical page (0 when invalid)
+  int len;    // valid tokens in the page (0 when invalid)
+};
+
+template <int MODE>
+__device__ __forceinline__ Item get_item(const AttendArgs& a, int i, int b, int bh, int L, int ns,
+                                         int cnt) {
+  Item it;
+  int lp;
+  if (MODE == kAttendSparse) {
+    if (i < cnt) {
+      lp = a.sel_pages[(size_t)bh * a.k_max + i];
+      if (lp < 0 || lp >= ns) {
+        set_error(a.err, LOCKS_DEVERR_SEL_PAGE);
+        lp = -1;
+      }
+    } else {
+      lp = ns + (i - cnt);
+    }
+  } else {
+    lp = i;
+  }
+  it.lp = lp;
+  it.phys = 0;
+  it.len = 0;
+  if (lp >= 0) {
+    int phys = a.block_table[(size_t)b * a.max_pages + lp];
+    if (phys < 0 || phys >= a.pages_total) {
+      set_error(a.err, LOCKS_DEVERR_BLOCK_TABLE);
+      it.lp = -1;
+    } else {
+      it.phys = phys;
+      int rem = L - lp * kPage;
+      it.len = rem < kPage ? rem : kPage;
+    }
+  }
+  return it;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_constant__ CUtensorMap tk,
+                                                                const __grid_constant__ CUtensorMap tv,
+                                                                const AttendArgs a) {
+  extern __shared__ uint8_t dyn_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t bars[kStages];
+  __shared__ float sm_m[kWarps][16], sm_l[kWarps][16];
+  __shared__ float2 sm_pl[kStages][kWarps][16];
+  __shared__ int s_last;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const int split = blockIdx.x, bh = blockIdx.y;
+  const int b = bh / a.num_kv_heads, hkv = bh % a.num_kv_heads;
+  const int G = a.group, Hq = a.num_kv_heads * G;
+
+  if (tid == 0) {
+    prefetch_tmap(&tk);
+    if (MODE != kAttendPageLse) prefetch_tmap(&tv);
+    for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  pdl_wait();
+
+  int L = a.seq_lens[b];
+  if (L < 0 || L > a.max_pages * kPage) {
+    if (tid == 0 && split == 0) set_error(a.err, LOCKS_DEVERR_LENGTHS);
+    L = L < 0 ? 0 : a.max_pages * kPage;
+  }
+  const int n_pages = (L + kPage - 1) / kPage;
+  int ns = 0, cnt = 0, n_items;
+  if (MODE == kAttendSparse) {
+    const int cap = min(L / kPage, a.max_pages);
+    ns = a.n_summarized[b];
+    ns = ns < 0 ? 0 : (ns > cap ? cap : ns);
+    cnt = a.sel_count[bh];
+    const int kcap = min(a.k_max, ns);
+    if (cnt < 0 || cnt > kcap) {
+      if (tid == 0) set_error(a.err, LOCKS_DEVERR_SEL_PAGE);
+      cnt = cnt < 0 ? 0 : kcap;
+    }
+    n_items = cnt + (n_pages - ns);
+  } else {
+    n_items = n_pages;
+  }
+  const int ipc = (n_items + a.n_splits - 1) / a.n_splits;
+  const int i0 = min(n_items, split * ipc), i1 = min(n_items, i0 + ipc);
+
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t tx_bytes = (MODE == kAttendPageLse) ? kTile : kStage;
+  auto issue = [&](int stage, int i) {
+    Item it = get_item<MODE>(a, i, b, bh, L, ns, cnt);
+    const int y = (it.phys * a.num_kv_heads + hkv) * kPage;
+    uint8_t* dst = smem + stage * kStage;
+    mbar_arrive_expect_tx(&bars[stage], tx_bytes);
+    tma_load_2d(dst, &tk, &bars[stage], 0, y);
+    tma_load_2d(dst + kHalfTile, &tk, &bars[stage], 64, y);
+    if (MODE != kAttendPageLse) {
+      tma_load_2d(dst + kTile, &tv, &bars[stage], 0, y);
+      tma_load_2d(dst + kTile + kHalfTile, &tv, &bars[stage], 64, y);
+    }
+  };
+  if (tid == 0) {
+    for (int s = 0; s < kStages && i0 + s < i1; ++s) issue(s, i0 + s);
+  }
+
+  // Q fragments (rows = heads of the group; rows >= G are zero)
+  uint32_t qf[8][4];
+  {
+    const uint16_t* qb = a.q + ((size_t)b * Hq + (size_t)hkv * G) * kHeadDim;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const int d0 = 16 * kk + 2 * c;
+      qf[kk][0] = (g < G) ? __ldg(reinterpret_cast<const uint32_t*>(qb + g * kHeadDim + d0)) : 0u;
+      qf[kk][1] = (g + 8 < G) ? __ldg(reinterpret_cast<const uint32_t*>(qb + (g + 8) * kHeadDim + d0)) : 0u;
+      qf[kk][2] = (g < G) ? __ldg(reinterpret_cast<const uint32_t*>(qb + g * kHeadDim + d0 + 8)) : 0u;
+      qf[kk][3] =
+          (g + 8 < G) ? __ldg(reinterpret_cast<const uint32_t*>(qb + (g + 8) * kHeadDim + d0 + 8)) : 0u;
+    }
+  }
+
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  bool failed = false;
+  float o[16][4];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+
+  for (int it = 0; i0 + it < i1; ++it) {
+    const int stage = it & 1;
+    const uint32_t parity = (it >> 1) & 1;
+    const Item item = get_item<MODE>(a, i0 + it, b, bh, L, ns, cnt);
+    const bool ok = mbar_wait(&bars[stage], parity);
+    if (__syncthreads_or(!ok)) {
+      if (tid == 0) set_error(a.err, kDevErrTimeout);
+      failed = true;
+      break;
+    }
+    const uint32_t kb = sbase + stage * kStage;
+    const uint32_t vb = kb + kTile;
+
+    // S = Q K^T for this warp's 16 tokens
+    float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    {
+      const int mi = lane >> 3;
+      const int row = 16 * warp + (mi >> 1) * 8 + (lane & 7);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        uint32_t b0, b1, b2, b3;
+        ldmatrix_x4(b0, b1, b2, b3, tile_addr(kb, row, 2 * kk + (mi & 1)));
+        mma_16816(s[0], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b0, b1);
+        mma_16816(s[1], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b2, b3);
+      }
+    }
+    const int len = item.len;
+    float tm0 = -INFINITY, tm1 = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int tok = 16 * warp + 8 * nt + 2 * c + e;
+        const bool valid = tok < len;
+        s[nt][e] = valid ? s[nt][e] * a.scale_log2 : -INFINITY;
+        s[nt][2 + e] = valid ? s[nt][2 + e] * a.scale_log2 : -INFINITY;
+        tm0 = fmaxf(tm0, s[nt][e]);
+        tm1 = fmaxf(tm1, s[nt][2 + e]);
+      }
+    }
+    tm0 = fmaxf(tm0, __shfl_xor_sync(0xffffffffu, tm0, 1));
+    tm0 = fmaxf(tm0, __shfl_xor_sync(0xffffffffu, tm0, 2));
+    tm1 = fmaxf(tm1, __shfl_xor_sync(0xffffffffu, tm1, 1));
+    tm1 = fmaxf(tm1, __shfl_xor_sync(0xffffffffu, tm1, 2));
+
+    if (MODE == kAttendPageLse) {
+      float p0 = 0.f, p1 = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          p0 += (tm0 == -INFINITY) ? 0.f : fast_exp2(s[nt][e] - tm0);
+          p1 += (tm1 == -INFINITY) ? 0.f : fast_exp2(s[nt][2 + e] - tm1);
+        }
+      p0 += __shfl_xor_sync(0xffffffffu, p0, 1);
+      p0 += __shfl_xor_sync(0xffffffffu, p0, 2);
+      p1 += __shfl_xor_sync(0xffffffffu, p1, 1);
+      p1 += __shfl_xor_sync(0xffffffffu, p1, 2);
+      if (c == 0) {
+        sm_pl[stage][warp][g] = make_float2(tm0, p0);
+        sm_pl[stage][warp][g + 8] = make_float2(tm1, p1);
+      }
+    } else {
+      const float mn0 = fmaxf(m0, tm0), mn1 = fmaxf(m1, tm1);
+      const float al0 = (mn0 == -INFINITY) ? 1.f : fast_exp2(m0 - mn0);
+      const float al1 = (mn1 == -INFINITY) ? 1.f : fast_exp2(m1 - mn1);
+      float p[2][4];
+      float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          p[nt][e] = (mn0 == -INFINITY) ? 0.f : fast_exp2(s[nt][e] - mn0);
+          p[nt][2 + e] = (mn1 == -INFINITY) ? 0.f : fast_exp2(s[nt][2 + e] - mn1);
+          ps0 += p[nt][e];
+          ps1 += p[nt][2 + e];
+        }
+      l0 = l0 * al0 + ps0;
+      l1 = l1 * al1 + ps1;
+      m0 = mn0;
+      m1 = mn1;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        o[i][0] *= al0;
+        o[i][1] *= al0;
+        o[i][2] *= al1;
+        o[i][3] *= al1;
+      }
+      // zero V rows past the sequence end (their slots may hold anything)
+      if (len < kPage) {
+        for (int row = max(len, 16 * warp); row < 16 * warp + 16; ++row) {
+          uint8_t* vrow = smem + stage * kStage + kTile + row * 128;
+          *reinterpret_cast<uint32_t*>(vrow + lane * 4) = 0u;
+          *reinterpret_cast<uint32_t*>(vrow + kHalfTile + lane * 4) = 0u;
+        }
+        __syncwarp();
+      }
+      const uint32_t pa0 = pack_bf16(p[0][0], p[0][1]);
+      const uint32_t pa1 = pack_bf16(p[0][2], p[0][3]);
+      const uint32_t pa2 = pack_bf16(p[1][0], p[1][1]);
+      const uint32_t pa3 = pack_bf16(p[1][2], p[1][3]);
+      const int mi = lane >> 3;
+      const int row = 16 * warp + (mi & 1) * 8 + (lane & 7);
+#pragma unroll
+      for (int dn = 0; dn < 8; ++dn) {
+        uint32_t v0, v1, v2, v3;
+        ldmatrix_x4_trans(v0, v1, v2, v3, tile_addr(vb, row, 2 * dn + (mi >> 1)));
+        mma_16816(o[2 * dn], pa0, pa1, pa2, pa3, v0, v1);
+        mma_16816(o[2 * dn + 1], pa0, pa1, pa2, pa3, v2, v3);
+      }
+    }
+
+    fence_proxy_async();
+    __syncthreads();
+    if (MODE == kAttendPageLse) {
+      if (tid < G && item.lp >= 0) {
+        float mm = -INFINITY, ll = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) lse2_merge(mm, ll, sm_pl[stage][w][tid].x, sm_pl[stage][w][tid].y);
+        a.page_lse[((size_t)b * Hq + (size_t)hkv * G + tid) * a.max_pages + item.lp] =
+            (mm == -INFINITY) ? -INFINITY : (mm + fast_log2(ll)) * kLn2;
+      }
+    }
+    if (tid == 0 && i0 + it + kStages < i1) issue(stage, i0 + it + kStages);
+  }
+
+  if (failed) {
+    // give copies still in flight a bounded time to land before exiting
+    if (tid == 0)
+      for (int s = 0; s < kStages; ++s) (void)mbar_wait(&bars[s], 0);
+    return;
+  }
+  pdl_launch_dependents();
+  if (MODE == kAttendPageLse) return;
+
+  // ---- merge the four warps ----
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+  float* so = reinterpret_cast<float*>(smem);  // [kWarps][16][kOStride], stage ring is free now
+  if (c == 0) {
+    sm_m[warp][g] = m0;
+    sm_l[warp][g] = l0;
+    sm_m[warp][g + 8] = m1;
+    sm_l[warp][g + 8] = l1;
+  }
+#pragma unroll
+  for (int nt = 0; nt < 16; ++nt) {
+    const int col = 8 * nt + 2 * c;
+    *reinterpret_cast<float2*>(so + (warp * 16 + g) * kOStride + col) = make_float2(o[nt][0], o[nt][1]);
+    *reinterpret_cast<float2*>(so + (warp * 16 + g + 8) * kOStride + col) = make_float2(o[nt][2], o[nt][3]);
+  }
+  __syncthreads();
+
+  const int d = tid;  // one output column per thread
+  const bool single = a.n_splits == 1;
+  for (int h = 0; h < G; ++h) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w][h]);
+    float Ls = 0.f, O = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float f = fast_exp2(sm_m[w][h] - M);
+        Ls += sm_l[w][h] * f;
+        O += so[(w * 16 + h) * kOStride + d] * f;
+      }
+    }
+    if (single) {
+      const size_t oi = ((size_t)b * Hq + (size_t)hkv * G + h);
+      const float val = Ls > 0.f ? O / Ls : 0.f;
+      a.out[oi * kHeadDim + d] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
+      if (a.lse && d == 0) a.lse[oi] = (Ls > 0.f) ? (M + fast_log2(Ls)) * kLn2 : -INFINITY;
+    } else {
+      const size_t pi = ((size_t)bh * a.n_splits + split) * G + h;
+      a.part_o[pi * kHeadDim + d] = O;
+      if (d == 0) a.part_ml[pi] = make_float2(M, Ls);
+    }
+  }
+  if (single) return;
+
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(a.counters + bh, 1u) == (unsigned)(a.n_splits - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  for (int h = 0; h < G; ++h) {
+    const size_t p0 = (size_t)bh * a.n_splits * G + h;
+    float M = -INFINITY;
+    for (int sp = 0; sp < a.n_splits; ++sp) M = fmaxf(M, __ldcg(a.part_ml + p0 + (size_t)sp * G).x);
+    float Ls = 0.f, O = 0.f;
+    if (M != -INFINITY) {
+      for (int sp = 0; sp < a.n_splits; ++sp) {
+        const float2 ml = __ldcg(a.part_ml + p0 + (size_t)sp * G);
+        const float f = fast_exp2(ml.x - M);
+        Ls += ml.y * f;
+        O += __ldcg(a.part_o + (p0 + (size_t)sp * G) * kHeadDim + d) * f;
+      }
+    }
+    const size_t oi = ((size_t)b * Hq + (size_t)hkv * G + h);
+    const float val = Ls > 0.f ? O / Ls : 0.f;
+    a.out[oi * kHeadDim + d] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
+    if (a.lse && d == 0) a.lse[oi] = (Ls > 0.f) ? (M + fast_log2(Ls)) * kLn2 : -INFINITY;
+  }
+  if (tid == 0) a.counters[bh] = 0;
+}
+
+template <int MODE>
+cudaError_t launch_mode(const AttendArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s,
+                        bool pdl) {
+  const size_t smem = kStages * kStage + 1024;
+  cudaError_t e = cudaFuncSetAttribute(attend_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.n_splits, a.batch * a.num_kv_heads, 1);
+  cfg.blockDim = dim3(kAttendThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, attend_kernel<MODE>, tk, tv, a);
+}
+
+}  // namespace
+
+cudaError_t launch_attend(const AttendArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, int mode,
+                          cudaStream_t s, bool pdl) {
+  switch (mode) {
+    case kAttendSparse: return launch_mode<kAttendSparse>(a, tk, tv, s, pdl);
+    case kAttendDense: return launch_mode<kAttendDense>(a, tk, tv, s, pdl);
+    default: return launch_mode<kAttendPageLse>(a, tk, tv, s, pdl);
+  }
+}
+
+}  // namespace locks

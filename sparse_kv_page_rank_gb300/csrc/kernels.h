@@ -1,0 +1,90 @@
+// Internal launch interface between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace locks {
+
+// Summary scan: page-mass estimates s_hat for every summarised page and head.
+struct ScanArgs {
+  const uint16_t* basis_t;     // bf16 [pages_total][Hkv][r][d]
+  const uint16_t* coeffs;      // bf16 [pages_total][Hkv][P][r]
+  const uint16_t* q;           // bf16 [B][Hq][d]
+  const int32_t* block_table;  // [B][max_pages]
+  const int32_t* seq_lens;     // [B]
+  const int32_t* n_summarized; // [B]
+  float* shat;                 // ws: [B*Hkv][max_pages][G] natural log
+  float2* part;                // ws: [B*Hkv][n_chunks][G] (max, sum) of base-2 LSE
+  float* page_lse;             // optional [B][Hq][max_pages]
+  int* err;
+  int batch, num_kv_heads, group, rank, max_pages, pages_total;
+  int chunk_pages, n_chunks;
+  float scale_log2;            // scale * log2(e)
+};
+
+// GSA scores + top-k (chunk-local candidates, merged by the last CTA).
+struct TopkArgs {
+  const float* shat;
+  const float2* part;
+  int n_scan_chunks;
+  const int32_t* seq_lens;
+  const int32_t* n_summarized;
+  uint32_t* cand_key;   // ws: [B*Hkv][n_chunks][k_max]
+  int32_t* cand_idx;    // ws: same
+  int32_t* cand_cnt;    // ws: [B*Hkv][n_chunks]
+  unsigned* counters;   // ws: [B*Hkv]
+  int32_t* sel_pages;   // [B*Hkv][k_max]
+  int32_t* sel_count;   // [B*Hkv]
+  int* err;
+  int batch, num_kv_heads, group, max_pages, k_max;
+  int chunk_pages, n_chunks;
+  size_t smem_keys;     // capacity (entries) of the dynamic key buffer
+};
+
+// Paged flash-decode over a page list (sparse), every page (dense), or the
+// exact per-page LSE of every page (page_lse mode).
+struct AttendArgs {
+  const uint16_t* q;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  const int32_t* n_summarized;
+  const int32_t* sel_pages;   // sparse mode only
+  const int32_t* sel_count;   // sparse mode only
+  uint16_t* out;              // bf16 [B][Hq][d]
+  float* lse;                 // optional [B][Hq]
+  float* page_lse;            // page_lse mode: [B][Hq][max_pages]
+  float* part_o;              // ws: [B*Hkv][n_splits][G][d]
+  float2* part_ml;            // ws: [B*Hkv][n_splits][G]
+  unsigned* counters;         // ws: [B*Hkv]
+  int* err;
+  int batch, num_kv_heads, group, max_pages, pages_total, k_max, n_splits;
+  float scale_log2;
+};
+
+enum AttendMode { kAttendSparse = 0, kAttendDense = 1, kAttendPageLse = 2 };
+
+// Summary builder.
+struct BuildArgs {
+  const uint16_t* k_pool;
+  void* basis_t;
+  void* coeffs;
+  const int32_t* page_ids;
+  int n, num_kv_heads, rank, pages_total, out_f32;
+  int* err;
+};
+
+cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s, bool pdl);
+cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s, bool pdl);
+cudaError_t launch_attend(const AttendArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
+                          int mode, cudaStream_t s, bool pdl);
+cudaError_t launch_build(const BuildArgs& a, cudaStream_t s);
+
+size_t topk_smem_bytes(size_t keys);
+constexpr int kScanThreads = 256;
+constexpr int kScanWarps = kScanThreads / 32;
+constexpr int kTopkThreads = 256;
+constexpr int kAttendThreads = 128;
+
+}  // namespace locks

@@ -1,0 +1,97 @@
+"""Device-side state of one paged cache for PyTorch callers.
+
+``LocksRuntime`` owns the torch tensors the C ABI reads (pools, block table,
+lengths, summaries, workspace), the C structs that point at them, and thin
+methods that call the entry points of ``locks``.  It computes nothing itself.
+"""
+
+from __future__ import annotations
+
+import torch
+
+from . import locks as L
+
+
+class LocksRuntime:
+    """Holds a paged cache on ``device`` and calls liblocks.so on it.
+
+    k_pool, v_pool: bf16 [pages_total][Hkv][64][128]; block_table int32
+    [B][max_pages]; seq_lens, n_summarized int32 [B].  Summaries are
+    allocated here (bf16 [pages_total][Hkv][rank][128] and [..][64][rank]).
+    """
+
+    def __init__(self, k_pool: torch.Tensor, v_pool: torch.Tensor, block_table: torch.Tensor,
+                 seq_lens: torch.Tensor, n_summarized: torch.Tensor, num_q_heads: int, rank: int,
+                 budget_tokens: int, scale: float = 0.0):
+        assert k_pool.dtype == torch.bfloat16 and v_pool.dtype == torch.bfloat16
+        assert block_table.dtype == torch.int32 and seq_lens.dtype == torch.int32
+        self.device = k_pool.device
+        self.k_pool, self.v_pool = k_pool, v_pool
+        self.block_table, self.seq_lens = block_table, seq_lens
+        self.n_summarized = n_summarized.to(torch.int32)
+        pt, hkv, P, d = k_pool.shape
+        self.batch = block_table.shape[0]
+        self.num_kv_heads, self.num_q_heads = hkv, num_q_heads
+        self.rank = rank
+        self.basis_t = torch.zeros((pt, hkv, rank, d), dtype=torch.bfloat16, device=self.device)
+        self.coeffs = torch.zeros((pt, hkv, P, rank), dtype=torch.bfloat16, device=self.device)
+        self.cache = L.make_cache(k_pool, v_pool, block_table, seq_lens, self.n_summarized)
+        self.summary = L.make_summary(self.basis_t, self.coeffs, rank)
+        self.params = L.make_params(num_q_heads, budget_tokens, scale)
+        self.k_max = min(budget_tokens // P, block_table.shape[1])
+        self.ws_bytes = L.locks_workspace_size(self.cache, self.summary, self.params)
+        self.ws = torch.empty(self.ws_bytes + 256, dtype=torch.uint8, device=self.device)
+        off = (-self.ws.data_ptr()) % 256
+        self.ws = self.ws[off:off + self.ws_bytes]
+        L.locks_workspace_init(self.ws, self.ws_bytes)
+        B = self.batch
+        self.sel_pages = torch.zeros((B, hkv, max(self.k_max, 1)), dtype=torch.int32, device=self.device)
+        self.sel_count = torch.zeros((B, hkv), dtype=torch.int32, device=self.device)
+        self.out = torch.zeros((B, num_q_heads, d), dtype=torch.bfloat16, device=self.device)
+        self.lse = torch.zeros((B, num_q_heads), dtype=torch.float32, device=self.device)
+
+    def set_summaries(self, basis_t: torch.Tensor, coeffs: torch.Tensor):
+        """Install externally computed summaries (same layouts)."""
+        self.basis_t.copy_(basis_t)
+        self.coeffs.copy_(coeffs)
+
+    def build_summaries(self, page_ids: torch.Tensor, stream=None):
+        ids = page_ids.to(device=self.device, dtype=torch.int32).contiguous()
+        L.locks_build_summaries(self.cache, self.summary, ids, ids.numel(), self.ws, self.ws_bytes, stream)
+
+    def select(self, q: torch.Tensor, page_lse: torch.Tensor | None = None, stream=None):
+        L.locks_select(self.cache, self.summary, self.params, q, self.sel_pages, self.sel_count, page_lse,
+                       self.ws, self.ws_bytes, stream)
+        return self.sel_pages, self.sel_count
+
+    def page_scores(self, q: torch.Tensor, page_lse: torch.Tensor, stream=None):
+        L.locks_page_scores(self.cache, self.summary, self.params, q, page_lse, self.ws, self.ws_bytes, stream)
+        return page_lse
+
+    def sparse_attend(self, q: torch.Tensor, stream=None):
+        L.locks_sparse_attend(self.cache, self.params, q, self.sel_pages, self.sel_count, self.out, self.lse,
+                              self.ws, self.ws_bytes, stream)
+        return self.out, self.lse
+
+    def decode_step(self, q: torch.Tensor, out=None, lse=None, keep_selection: bool = True, stream=None):
+        out = self.out if out is None else out
+        lse = self.lse if lse is None else lse
+        sp, sc = (self.sel_pages, self.sel_count) if keep_selection else (None, None)
+        L.locks_decode_step(self.cache, self.summary, self.params, q, out, lse, sp, sc, self.ws,
+                            self.ws_bytes, stream)
+        return out, lse
+
+    def dense_decode(self, q: torch.Tensor, out=None, lse=None, stream=None):
+        out = self.out if out is None else out
+        lse = self.lse if lse is None else lse
+        L.locks_dense_decode(self.cache, self.params, q, out, lse, self.ws, self.ws_bytes, stream)
+        return out, lse
+
+    def exact_page_lse(self, q: torch.Tensor, stream=None) -> torch.Tensor:
+        pl = torch.full((self.batch, self.num_q_heads, self.block_table.shape[1]), float("nan"),
+                        dtype=torch.float32, device=self.device)
+        L.locks_exact_page_lse(self.cache, self.params, q, pl, stream)
+        return pl
+
+    def device_error(self, stream=None) -> int:
+        return L.locks_get_device_error(self.ws, stream)

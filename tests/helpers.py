@@ -1,0 +1,77 @@
+"""Shared helpers of the test suite: moving synthetic cases to the GPU and
+computing oracle summaries in the library's storage layout (test-side
+marshalling only; no method arithmetic beyond calling the oracle)."""
+
+from __future__ import annotations
+
+import numpy as np
+
+import oracle as O
+from synth import bf16_bits, bf16_to_f32
+
+
+def oracle_summaries_bf16(case, r: int, pages=None):
+    """Oracle rank-r summaries of every full page (or the listed physical
+    pages), rounded to bf16, in the C-ABI layouts:
+    basis_t uint16 [pages_total][Hkv][r][d], coeffs uint16 [pages_total][Hkv][P][r]."""
+    kf = O.bf16_widen(case.k_pool)
+    pt, hkv, P, d = case.k_pool.shape
+    basis_t = np.zeros((pt, hkv, r, d), dtype=np.uint16)
+    coeffs = np.zeros((pt, hkv, P, r), dtype=np.uint16)
+    if pages is None:
+        pages = []
+        for b in range(case.batch):
+            pages.extend(int(x) for x in case.block_table[b, :case.n_full_pages(b)])
+    for p in pages:
+        for h in range(hkv):
+            V, C, _, _ = O.page_summary(kf[p, h], r)
+            basis_t[p, h] = bf16_bits(V.T.astype(np.float32))
+            coeffs[p, h] = bf16_bits(C.astype(np.float32))
+    return basis_t, coeffs
+
+
+def oracle_layout_from_abi(basis_t_u16, coeffs_u16):
+    """ABI layout (bf16 bits) -> oracle layout float64: basis [..][d][r], coeffs [..][P][r]."""
+    basis = np.swapaxes(bf16_to_f32(basis_t_u16).astype(np.float64), -1, -2)
+    coeffs = bf16_to_f32(coeffs_u16).astype(np.float64)
+    return basis, coeffs
+
+
+def to_torch_bf16(arr_u16, device):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(arr_u16).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def torch_bf16_to_u16(t):
+    import torch
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def make_runtime(case, rank: int, budget_tokens: int, n_summarized=None, device="cuda"):
+    import torch
+    from sparse_kv_page_rank_gb300.runtime import LocksRuntime
+    if n_summarized is None:
+        n_summarized = [case.n_full_pages(b) for b in range(case.batch)]
+    rt = LocksRuntime(to_torch_bf16(case.k_pool, device), to_torch_bf16(case.v_pool, device),
+                      torch.from_numpy(case.block_table).to(device),
+                      torch.from_numpy(case.seq_lens).to(device),
+                      torch.tensor(np.asarray(n_summarized, dtype=np.int32)).to(device),
+                      case.num_q_heads, rank, budget_tokens)
+    q = to_torch_bf16(case.q, device)
+    return rt, q
+
+
+def cut_band_ok(sigma_oracle: np.ndarray, sel_gpu, sel_oracle, k: int, band: float = 1e-4):
+    """Selection comparison outside the band |sigma - sigma_(k)| <= band around
+    the cut.  Returns (ok, detail)."""
+    n = sigma_oracle.size
+    k = min(k, n)
+    if k == 0:
+        return len(sel_gpu) == 0, "k=0"
+    if k >= n:
+        return sorted(sel_gpu) == list(range(n)), "all"
+    kth = np.sort(sigma_oracle)[::-1][k - 1]
+    near = set(np.nonzero(np.abs(sigma_oracle - kth) <= band)[0].tolist())
+    a = set(int(x) for x in sel_gpu) - near
+    b = set(int(x) for x in sel_oracle) - near
+    return a == b and len(sel_gpu) == k, f"gpu-only={sorted(a - b)} oracle-only={sorted(b - a)} near={len(near)}"
