@@ -31,11 +31,12 @@ int device_sm_count() {
 }
 
 struct Plan {
+  bool ok = true;  // false: shapes beyond what the launch plan supports
   int G = 0, Hq = 0, BH = 0, k_max = 0;
   int scan_chunk = 0, n_scan = 0;
   int tk_chunk = 0, n_tk = 0;
   size_t tk_keys = 0;
-  int sparse_splits = 0, dense_splits = 0, max_splits = 0;
+  int sparse_cluster = 1, dense_cluster = 1, dense_nc = 1, lse_splits = 1;
   size_t off_err = 0, off_cnt_tk = 0, off_cnt_att = 0, off_shat = 0, off_part = 0, off_ckey = 0,
          off_cidx = 0, off_ccnt = 0, off_sel = 0, off_selcnt = 0, off_pml = 0, off_po = 0, total = 0;
 };
@@ -51,7 +52,7 @@ locks_status_t check_cache(const locks_cache_t* c, bool need_kv) {
       return LOCKS_ERR_INVALID_ARG;
   }
   // TMA row coordinate and 32-bit page-head offsets
-  if ((long long)c->pages_total * c->num_kv_heads * kPage > 0x7fffffffLL) return LOCKS_ERR_UNSUPPORTED;
+  if ((long long)c->pages_total * c->num_kv_heads * kPage > 0x7fffffffLL) return LOCKS_ERR_UNSUPPORTED;  // >= basis rows
   if ((long long)c->max_pages * kPage > 0x7fffffffLL) return LOCKS_ERR_UNSUPPORTED;
   return LOCKS_OK;
 }
@@ -97,30 +98,52 @@ Plan make_plan(const locks_cache_t* c, const locks_params_t* p) {
     pl.scan_chunk = (int)std::min<long long>(per, (long long)c->max_pages + kScanWarps);
     pl.n_scan = (c->max_pages + pl.scan_chunk - 1) / pl.scan_chunk;
   }
-  // top-k: chunks of 1024 pages; grow chunks while candidates would overflow
+  // top-k: each CTA scores a fixed chunk of pages (its threads hold the
+  // pages' s_hat rows in registers); the last CTA of a problem merges the
+  // chunks' candidates (at most 64 chunks)
   {
-    int chunk = 1024;
-    int n = (c->max_pages + chunk - 1) / chunk;
-    while (n > 1 && (long long)n * std::max(pl.k_max, 1) > 16384 && chunk < 16384) {
-      chunk *= 2;
-      n = (c->max_pages + chunk - 1) / chunk;
-    }
+    const int chunk = topk_pages_per_cta(pl.G);
+    const int n = (c->max_pages + chunk - 1) / chunk;
     pl.tk_chunk = chunk;
     pl.n_tk = n;
     pl.tk_keys = std::max<size_t>((size_t)std::min(chunk, c->max_pages), (size_t)n * std::max(pl.k_max, 1));
+    if (n > 64 || topk_smem_bytes(pl.tk_keys) > 200 * 1024) pl.ok = false;
   }
-  // attention: about three resident CTAs per SM
+  // attention: one thread-block cluster per problem for the sparse step
+  // (selected pages + a short tail spread over its CTAs, merged on chip);
+  // several clusters per problem for the dense decode, about three resident
+  // CTAs per SM
   {
     const long long target = 3LL * sms;
+    const int cs_sparse = attend_max_cluster(kAttendSparse);
+    const int cs_dense = attend_max_cluster(kAttendDense);
     const long long items = (long long)pl.k_max + 2;
-    if (BH * items <= target)
-      pl.sparse_splits = (int)items;
-    else
-      pl.sparse_splits = (int)std::max<long long>(1, target / BH);
-    pl.sparse_splits = std::max(1, std::min<int>(pl.sparse_splits, (int)items));
-    long long ds = (target + BH - 1) / BH;
-    pl.dense_splits = (int)std::max<long long>(1, std::min<long long>(ds, c->max_pages));
-    pl.max_splits = std::max(pl.sparse_splits, pl.dense_splits);
+    int cs = 1;
+    while (cs * 2 <= cs_sparse && cs * 2 <= items) cs *= 2;
+    while (cs > 1 && BH * cs > 2 * target) cs /= 2;
+    pl.sparse_cluster = cs;
+    // dense: the (cluster, clusters-per-problem) shape with the most CTAs
+    // that still fits in one wave of `target` resident CTAs
+    long long best = -1;
+    for (int csd = cs_dense; csd >= 1; csd /= 2) {
+      if (csd > c->max_pages) continue;
+      long long nc = target / (BH * csd);
+      nc = std::max<long long>(1, std::min<long long>(nc, (c->max_pages + csd - 1) / csd));
+      const long long ctas = BH * csd * nc;
+      // prefer large clusters (cheap on-chip merges) unless a smaller one
+      // fills the wave clearly better
+      if (ctas <= target && (best < 0 || ctas * 10 > best * 12)) {
+        best = ctas;
+        pl.dense_cluster = csd;
+        pl.dense_nc = (int)nc;
+      }
+    }
+    if (best < 0) {
+      pl.dense_cluster = 1;
+      pl.dense_nc = 1;
+    }
+    long long ls = (target + BH - 1) / BH;
+    pl.lse_splits = (int)std::max<long long>(1, std::min<long long>(ls, c->max_pages));
   }
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -138,8 +161,8 @@ Plan make_plan(const locks_cache_t* c, const locks_params_t* p) {
   pl.off_ccnt = take(sizeof(int32_t) * BH * pl.n_tk);
   pl.off_sel = take(sizeof(int32_t) * BH * std::max(pl.k_max, 1));
   pl.off_selcnt = take(sizeof(int32_t) * BH);
-  pl.off_pml = take(sizeof(float2) * BH * pl.max_splits * pl.G);
-  pl.off_po = take(sizeof(float) * BH * pl.max_splits * pl.G * kHeadDim);
+  pl.off_pml = take(sizeof(float2) * BH * pl.dense_nc * pl.G);
+  pl.off_po = take(sizeof(float) * BH * pl.dense_nc * pl.G * kHeadDim);
   pl.total = off;
   return pl;
 }
@@ -168,19 +191,24 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D view of a pool: rows = pages_total * Hkv * P tokens, 128 bf16 columns;
-// 64 x 64 boxes with 128-byte swizzle.
-bool encode_pool(CUtensorMap* m, const void* pool, const locks_cache_t* c) {
+// 2-D view of a pool of 128-column bf16 rows (rows = pages_total * Hkv *
+// rows_per_page); 64-column boxes of box_rows rows with 128-byte swizzle.
+bool encode_rows(CUtensorMap* m, const void* pool, const locks_cache_t* c, int rows_per_page, int box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)c->pages_total * c->num_kv_heads * kPage};
+  cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)c->pages_total * c->num_kv_heads * rows_per_page};
   cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
-  cuuint32_t box[2] = {64, 64};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// K or V pool: 64 x 64 boxes (one page-head is two boxes).
+bool encode_pool(CUtensorMap* m, const void* pool, const locks_cache_t* c) {
+  return encode_rows(m, pool, c, kPage, 64);
 }
 
 locks_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? LOCKS_OK : LOCKS_ERR_CUDA; }
@@ -238,7 +266,7 @@ locks_status_t run_select(const locks_cache_t* c, const locks_summary_t* s, cons
 
 locks_status_t run_attend(const locks_cache_t* c, const locks_params_t* p, const Plan& pl, const void* q,
                           const int32_t* sel, const int32_t* selcnt, void* out, float* lse, float* page_lse,
-                          void* ws, int mode, cudaStream_t st) {
+                          void* ws, int mode, cudaStream_t st, bool inputs_early = false) {
   CUtensorMap tk, tv;
   std::memset(&tk, 0, sizeof(tk));
   std::memset(&tv, 0, sizeof(tv));
@@ -264,8 +292,18 @@ locks_status_t run_attend(const locks_cache_t* c, const locks_params_t* p, const
   a.max_pages = c->max_pages;
   a.pages_total = c->pages_total;
   a.k_max = pl.k_max;
-  a.n_splits = mode == kAttendSparse ? pl.sparse_splits : pl.dense_splits;
+  if (mode == kAttendSparse) {
+    a.cluster = pl.sparse_cluster;
+    a.n_splits = pl.sparse_cluster;
+  } else if (mode == kAttendDense) {
+    a.cluster = pl.dense_cluster;
+    a.n_splits = pl.dense_cluster * pl.dense_nc;
+  } else {
+    a.cluster = 1;
+    a.n_splits = pl.lse_splits;
+  }
   a.scale_log2 = scale_of(p) * kLog2e;
+  a.inputs_early = inputs_early ? 1 : 0;
   return cuda_status(launch_attend(a, tk, tv, mode, st, true));
 }
 
@@ -292,7 +330,9 @@ locks_status_t locks_workspace_size(const locks_cache_t* cache, const locks_summ
   locks_status_t st = check_cache(cache, false);
   if (st != LOCKS_OK) return st;
   if ((st = check_params(cache, params)) != LOCKS_OK) return st;
-  *bytes = make_plan(cache, params).total;
+  Plan pl = make_plan(cache, params);
+  if (!pl.ok) return LOCKS_ERR_UNSUPPORTED;
+  *bytes = pl.total;
   return LOCKS_OK;
 }
 
@@ -336,6 +376,7 @@ locks_status_t locks_select(const locks_cache_t* cache, const locks_summary_t* s
   if ((st = check_summary(summary, true)) != LOCKS_OK) return st;
   if (!q || !sel_pages || !sel_count) return LOCKS_ERR_INVALID_ARG;
   Plan pl = make_plan(cache, params);
+  if (!pl.ok) return LOCKS_ERR_UNSUPPORTED;
   if ((st = check_ws(ws, ws_bytes, pl)) != LOCKS_OK) return st;
   return run_select(cache, summary, params, pl, q, sel_pages, sel_count, page_lse, ws,
                     static_cast<cudaStream_t>(stream));
@@ -351,6 +392,7 @@ locks_status_t locks_page_scores(const locks_cache_t* cache, const locks_summary
   if ((st = check_summary(summary, true)) != LOCKS_OK) return st;
   if (!q || !page_lse) return LOCKS_ERR_INVALID_ARG;
   Plan pl = make_plan(cache, params);
+  if (!pl.ok) return LOCKS_ERR_UNSUPPORTED;
   if ((st = check_ws(ws, ws_bytes, pl)) != LOCKS_OK) return st;
   return run_select(cache, summary, params, pl, q, nullptr, nullptr, page_lse, ws,
                     static_cast<cudaStream_t>(stream));
@@ -365,6 +407,7 @@ locks_status_t locks_sparse_attend(const locks_cache_t* cache, const locks_param
   if ((st = check_params(cache, params)) != LOCKS_OK) return st;
   if (!q || !sel_pages || !sel_count || !out) return LOCKS_ERR_INVALID_ARG;
   Plan pl = make_plan(cache, params);
+  if (!pl.ok) return LOCKS_ERR_UNSUPPORTED;
   if ((st = check_ws(ws, ws_bytes, pl)) != LOCKS_OK) return st;
   return run_attend(cache, params, pl, q, sel_pages, sel_count, out, lse, nullptr, ws, kAttendSparse,
                     static_cast<cudaStream_t>(stream));
@@ -381,12 +424,13 @@ locks_status_t locks_decode_step(const locks_cache_t* cache, const locks_summary
   if ((st = check_summary(summary, true)) != LOCKS_OK) return st;
   if (!q || !out || ((sel_pages == nullptr) != (sel_count == nullptr))) return LOCKS_ERR_INVALID_ARG;
   Plan pl = make_plan(cache, params);
+  if (!pl.ok) return LOCKS_ERR_UNSUPPORTED;
   if ((st = check_ws(ws, ws_bytes, pl)) != LOCKS_OK) return st;
   int32_t* sel = sel_pages ? sel_pages : at<int32_t>(ws, pl.off_sel);
   int32_t* cnt = sel_count ? sel_count : at<int32_t>(ws, pl.off_selcnt);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if ((st = run_select(cache, summary, params, pl, q, sel, cnt, nullptr, ws, s)) != LOCKS_OK) return st;
-  return run_attend(cache, params, pl, q, sel, cnt, out, lse, nullptr, ws, kAttendSparse, s);
+  return run_attend(cache, params, pl, q, sel, cnt, out, lse, nullptr, ws, kAttendSparse, s, true);
 }
 
 locks_status_t locks_dense_decode(const locks_cache_t* cache, const locks_params_t* params, const void* q,
@@ -396,6 +440,7 @@ locks_status_t locks_dense_decode(const locks_cache_t* cache, const locks_params
   if ((st = check_params(cache, params)) != LOCKS_OK) return st;
   if (!q || !out) return LOCKS_ERR_INVALID_ARG;
   Plan pl = make_plan(cache, params);
+  if (!pl.ok) return LOCKS_ERR_UNSUPPORTED;
   if ((st = check_ws(ws, ws_bytes, pl)) != LOCKS_OK) return st;
   return run_attend(cache, params, pl, q, nullptr, nullptr, out, lse, nullptr, ws, kAttendDense,
                     static_cast<cudaStream_t>(stream));

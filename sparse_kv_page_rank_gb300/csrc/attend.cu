@@ -7,19 +7,25 @@
 // per-page log-sum-exp that reads every key (the "read-every-key exact-LSE
 // oracle" the abstract measures selection against).
 //
-// Work split: grid (n_splits, B*Hkv).  The page list of problem bh
-// (sel_pages[0..cnt) then the tail pages, or every page) is cut into n_splits
-// contiguous ranges.  A CTA of four warps streams its pages through a
-// two-stage shared-memory ring: one thread issues 2-D TMA loads
-// (cp.async.bulk.tensor, 64 x 64 bf16 boxes, 128-byte swizzle) of the page's
-// K and V tiles (16 KiB each) and an mbarrier with a transaction count tells
-// the warps when they have landed.  Warp w owns tokens 16w..16w+15 of every
-// page: S = Q K^T on tensor cores (m16n8k16, M = the G <= 16 query heads of
-// the group), an online base-2 softmax in registers, then O += P V with P
-// reused from the accumulator layout and V fragments read by ldmatrix.trans.
-// Partial results (max, sum, O) of the four warps are merged in shared memory;
-// the CTAs of one problem are merged by the last CTA to finish (atomic ticket,
-// no spinning), which writes o (bf16) and lse (natural log).
+// Work split: grid (CS * NC, B*Hkv) with thread-block clusters of CS CTAs
+// (NC clusters per problem).  The page list of problem bh (sel_pages[0..cnt)
+// then the tail pages, or every page) is cut into CS*NC contiguous ranges.  A
+// CTA of four warps streams its pages through a shared-memory ring: one thread
+// issues 2-D TMA loads (cp.async.bulk.tensor, 64 x 64 bf16 boxes, 128-byte
+// swizzle) of the page's K and V tiles (16 KiB each) and an mbarrier with a
+// transaction count tells the warps when they have landed.  Warp w owns tokens
+// 16w..16w+15 of every page: S = Q K^T on tensor cores (m16n8k16, M = the
+// G <= 16 query heads of the group), an online base-2 softmax in registers,
+// then O += P V with P reused from the accumulator layout and V fragments read
+// by ldmatrix.trans.
+//
+// Merging partial softmax states (max m, sum l, O): the four warps of a CTA
+// in shared memory; the CTAs of a cluster through distributed shared memory
+// (after a cluster barrier, CTA rank c reads every CTA's state for output
+// columns [c*128/CS, (c+1)*128/CS)); with NC > 1 the clusters of a problem
+// write their partial to the workspace and the last cluster to finish (atomic
+// ticket, no waiting) merges them, again one column slice per CTA.  The
+// result is o (bf16) and lse (natural log).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -31,8 +37,8 @@ constexpr int kWarps = kAttendThreads / 32;
 constexpr int kHalfTile = 64 * 128;        // bytes of one 64-row x 64-col bf16 box
 constexpr int kTile = 2 * kHalfTile;       // one page-head of K (or V): 16 KiB
 constexpr int kStage = 2 * kTile;          // K + V
-constexpr int kStages = 2;
-constexpr int kOStride = 132;              // padded row of the O merge buffer (floats)
+constexpr int kOStride = 132;              // padded row of the per-warp O buffer (floats)
+constexpr int kOctaOff = kWarps * 16 * kOStride * 4;  // CTA-level O [16][128] after the warp buffers
 
 __device__ __forceinline__ uint32_t tile_addr(uint32_t base, int row, int chunk16) {
   // 128B swizzle: 16-byte chunk index XOR (row mod 8) within each 128-byte row
@@ -81,16 +87,22 @@ __device__ __forceinline__ Item get_item(const AttendArgs& a, int i, int b, int 
   return it;
 }
 
-template <int MODE>
+template <int MODE, int STAGES>
 __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_constant__ CUtensorMap tk,
                                                                 const __grid_constant__ CUtensorMap tv,
                                                                 const AttendArgs a) {
   extern __shared__ uint8_t dyn_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t bars[kStages];
+  __shared__ __align__(8) uint64_t bars[STAGES];
   __shared__ float sm_m[kWarps][16], sm_l[kWarps][16];
-  __shared__ float2 sm_pl[kStages][kWarps][16];
+  __shared__ float2 sm_pl[STAGES][kWarps][16];
+  __shared__ float cta_m[16], cta_l[16];
+  __shared__ float rk_m[16][16], rk_l[16][16];  // (rank, head) states of the cluster
   __shared__ int s_last;
+  // items of this CTA resolved in parallel (one per thread, in batches)
+  // (double-buffered so that the next batch can be resolved while the
+  // current one is still being consumed)
+  __shared__ int it_phys[2][kAttendThreads], it_len[2][kAttendThreads], it_lp[2][kAttendThreads];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, c = lane & 3;
@@ -98,57 +110,19 @@ __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_con
   const int b = bh / a.num_kv_heads, hkv = bh % a.num_kv_heads;
   const int G = a.group, Hq = a.num_kv_heads * G;
 
+  if (MODE == kAttendSparse) trace_mark(a.err, kTrAttEnter, true);
   if (tid == 0) {
     prefetch_tmap(&tk);
     if (MODE != kAttendPageLse) prefetch_tmap(&tv);
-    for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+    for (int s = 0; s < STAGES; ++s) mbar_init(&bars[s], 1);
     fence_mbar_init();
   }
   __syncthreads();
 
-  pdl_wait();
-
-  int L = a.seq_lens[b];
-  if (L < 0 || L > a.max_pages * kPage) {
-    if (tid == 0 && split == 0) set_error(a.err, LOCKS_DEVERR_LENGTHS);
-    L = L < 0 ? 0 : a.max_pages * kPage;
-  }
-  const int n_pages = (L + kPage - 1) / kPage;
-  int ns = 0, cnt = 0, n_items;
-  if (MODE == kAttendSparse) {
-    const int cap = min(L / kPage, a.max_pages);
-    ns = a.n_summarized[b];
-    ns = ns < 0 ? 0 : (ns > cap ? cap : ns);
-    cnt = a.sel_count[bh];
-    const int kcap = min(a.k_max, ns);
-    if (cnt < 0 || cnt > kcap) {
-      if (tid == 0) set_error(a.err, LOCKS_DEVERR_SEL_PAGE);
-      cnt = cnt < 0 ? 0 : kcap;
-    }
-    n_items = cnt + (n_pages - ns);
-  } else {
-    n_items = n_pages;
-  }
-  const int ipc = (n_items + a.n_splits - 1) / a.n_splits;
-  const int i0 = min(n_items, split * ipc), i1 = min(n_items, i0 + ipc);
-
-  const uint32_t sbase = smem_u32(smem);
-  const uint32_t tx_bytes = (MODE == kAttendPageLse) ? kTile : kStage;
-  auto issue = [&](int stage, int i) {
-    Item it = get_item<MODE>(a, i, b, bh, L, ns, cnt);
-    const int y = (it.phys * a.num_kv_heads + hkv) * kPage;
-    uint8_t* dst = smem + stage * kStage;
-    mbar_arrive_expect_tx(&bars[stage], tx_bytes);
-    tma_load_2d(dst, &tk, &bars[stage], 0, y);
-    tma_load_2d(dst + kHalfTile, &tk, &bars[stage], 64, y);
-    if (MODE != kAttendPageLse) {
-      tma_load_2d(dst + kTile, &tv, &bars[stage], 0, y);
-      tma_load_2d(dst + kTile + kHalfTile, &tv, &bars[stage], 64, y);
-    }
-  };
-  if (tid == 0) {
-    for (int s = 0; s < kStages && i0 + s < i1; ++s) issue(s, i0 + s);
-  }
+  // Inside the fused step the step's own inputs (q, lengths, block table) were
+  // written before its first kernel started, so they can be read while the
+  // selection is still being computed; the selection itself only after the wait.
+  if (!a.inputs_early) pdl_wait();
 
   // Q fragments (rows = heads of the group; rows >= G are zero)
   uint32_t qf[8][4];
@@ -164,23 +138,95 @@ __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_con
           (g + 8 < G) ? __ldg(reinterpret_cast<const uint32_t*>(qb + (g + 8) * kHeadDim + d0 + 8)) : 0u;
     }
   }
+  int L = a.seq_lens[b];
+  const int ns_raw = (MODE == kAttendSparse) ? a.n_summarized[b] : 0;
+  if (MODE == kAttendSparse && a.inputs_early) {
+    // warm L2 with this sequence's block-table row while the selection is
+    // still being computed (the entries are looked up right after the wait)
+    const char* row = reinterpret_cast<const char*>(a.block_table + (size_t)b * a.max_pages);
+    const int lines = (a.max_pages * 4 + 127) / 128;
+    for (int li = tid; li < lines; li += kAttendThreads)
+      asm volatile("prefetch.global.L2 [%0];\n" ::"l"(row + (size_t)li * 128));
+  }
+  if (a.inputs_early) pdl_wait();
+  if (MODE == kAttendSparse) trace_mark(a.err, kTrAttWait, true);
+
+  if (L < 0 || L > a.max_pages * kPage) {
+    if (tid == 0 && split == 0) set_error(a.err, LOCKS_DEVERR_LENGTHS);
+    L = L < 0 ? 0 : a.max_pages * kPage;
+  }
+  const int n_pages = (L + kPage - 1) / kPage;
+  int ns = 0, cnt = 0, n_items;
+  if (MODE == kAttendSparse) {
+    const int cap = min(L / kPage, a.max_pages);
+    ns = ns_raw < 0 ? 0 : (ns_raw > cap ? cap : ns_raw);
+    cnt = a.sel_count[bh];
+    const int kcap = min(a.k_max, ns);
+    if (cnt < 0 || cnt > kcap) {
+      if (tid == 0) set_error(a.err, LOCKS_DEVERR_SEL_PAGE);
+      cnt = cnt < 0 ? 0 : kcap;
+    }
+    n_items = cnt + (n_pages - ns);
+  } else {
+    n_items = n_pages;
+  }
+  const int ipc = (n_items + a.n_splits - 1) / a.n_splits;
+  const int i0 = min(n_items, split * ipc), i1 = min(n_items, i0 + ipc);
+
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t tx_bytes = (MODE == kAttendPageLse) ? kTile : kStage;
+  // resolve items [base, base + kAttendThreads) of this CTA: selection entry
+  // and block-table entry, all threads at once
+  auto resolve = [&](int base) {
+    const int i = i0 + base + tid;
+    const int buf = (base / kAttendThreads) & 1;
+    if (i < i1) {
+      const Item it = get_item<MODE>(a, i, b, bh, L, ns, cnt);
+      it_phys[buf][tid] = it.phys;
+      it_len[buf][tid] = it.len;
+      it_lp[buf][tid] = it.lp;
+    }
+  };
+  resolve(0);
+  __syncthreads();
+  if (MODE == kAttendSparse) trace_mark(a.err, kTrAttResolved, false);
+  // thread 0 only; item (i - i0) must lie in the resolved batch
+  auto issue = [&](int stage, int i) {
+    const int k = i - i0;
+    const int y = (it_phys[(k / kAttendThreads) & 1][k % kAttendThreads] * a.num_kv_heads + hkv) * kPage;
+    uint8_t* dst = smem + stage * kStage;
+    mbar_arrive_expect_tx(&bars[stage], tx_bytes);
+    tma_load_2d(dst, &tk, &bars[stage], 0, y);
+    tma_load_2d(dst + kHalfTile, &tk, &bars[stage], 64, y);
+    if (MODE != kAttendPageLse) {
+      tma_load_2d(dst + kTile, &tv, &bars[stage], 0, y);
+      tma_load_2d(dst + kTile + kHalfTile, &tv, &bars[stage], 64, y);
+    }
+  };
+  if (tid == 0) {
+    for (int s = 0; s < STAGES && i0 + s < i1 && s < kAttendThreads; ++s) issue(s, i0 + s);
+  }
 
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   bool failed = false;
+  int consumed = 0;
   float o[16][4];
 #pragma unroll
   for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 
   for (int it = 0; i0 + it < i1; ++it) {
-    const int stage = it & 1;
-    const uint32_t parity = (it >> 1) & 1;
-    const Item item = get_item<MODE>(a, i0 + it, b, bh, L, ns, cnt);
+    const int stage = it % STAGES;
+    const uint32_t parity = (it / STAGES) & 1;
+    const int item_len = it_len[(it / kAttendThreads) & 1][it % kAttendThreads];
+    const int item_lp = it_lp[(it / kAttendThreads) & 1][it % kAttendThreads];
     const bool ok = mbar_wait(&bars[stage], parity);
     if (__syncthreads_or(!ok)) {
       if (tid == 0) set_error(a.err, kDevErrTimeout);
       failed = true;
       break;
     }
+    consumed = it + 1;
+    if (MODE == kAttendSparse && it == 0) trace_mark(a.err, kTrAttFirstData, false);
     const uint32_t kb = sbase + stage * kStage;
     const uint32_t vb = kb + kTile;
 
@@ -197,7 +243,7 @@ __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_con
         mma_16816(s[1], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b2, b3);
       }
     }
-    const int len = item.len;
+    const int len = item_len;
     float tm0 = -INFINITY, tm1 = -INFINITY;
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
@@ -286,32 +332,44 @@ __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_con
     fence_proxy_async();
     __syncthreads();
     if (MODE == kAttendPageLse) {
-      if (tid < G && item.lp >= 0) {
+      if (tid < G && item_lp >= 0) {
         float mm = -INFINITY, ll = 0.f;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) lse2_merge(mm, ll, sm_pl[stage][w][tid].x, sm_pl[stage][w][tid].y);
-        a.page_lse[((size_t)b * Hq + (size_t)hkv * G + tid) * a.max_pages + item.lp] =
+        a.page_lse[((size_t)b * Hq + (size_t)hkv * G + tid) * a.max_pages + item_lp] =
             (mm == -INFINITY) ? -INFINITY : (mm + fast_log2(ll)) * kLn2;
       }
     }
-    if (tid == 0 && i0 + it + kStages < i1) issue(stage, i0 + it + kStages);
+    // next batch of item descriptors once the current one has been issued
+    const int nxt = it + STAGES;
+    if (nxt % kAttendThreads == 0 && i0 + nxt < i1) {
+      resolve(nxt);
+      __syncthreads();
+    }
+    if (tid == 0 && i0 + nxt < i1) issue(stage, i0 + nxt);
   }
 
   if (failed) {
-    // give copies still in flight a bounded time to land before exiting
-    if (tid == 0)
-      for (int s = 0; s < kStages; ++s) (void)mbar_wait(&bars[s], 0);
-    return;
+    // give copies still in flight a bounded time to land before the ring is reused
+    if (tid == 0) {
+      for (int it = consumed; it < consumed + STAGES && i0 + it < i1; ++it)
+        (void)mbar_wait(&bars[it % STAGES], (it / STAGES) & 1);
+    }
+    __syncthreads();
+    m0 = m1 = -INFINITY;
+    l0 = l1 = 0.f;
   }
   pdl_launch_dependents();
   if (MODE == kAttendPageLse) return;
+  if (MODE == kAttendSparse) trace_mark(a.err, kTrAttLooped, false);
 
-  // ---- merge the four warps ----
+  // ---- merge the four warps of this CTA ----
   l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
   l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-  float* so = reinterpret_cast<float*>(smem);  // [kWarps][16][kOStride], stage ring is free now
+  float* so = reinterpret_cast<float*>(smem);              // [kWarps][16][kOStride]
+  float* octa = reinterpret_cast<float*>(smem + kOctaOff);  // [16][128]
   if (c == 0) {
     sm_m[warp][g] = m0;
     sm_l[warp][g] = l0;
@@ -325,10 +383,8 @@ __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_con
     *reinterpret_cast<float2*>(so + (warp * 16 + g + 8) * kOStride + col) = make_float2(o[nt][2], o[nt][3]);
   }
   __syncthreads();
-
-  const int d = tid;  // one output column per thread
-  const bool single = a.n_splits == 1;
-  for (int h = 0; h < G; ++h) {
+  for (int e = tid; e < G * kHeadDim; e += kAttendThreads) {
+    const int h = e / kHeadDim, d = e % kHeadDim;
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w][h]);
@@ -341,74 +397,186 @@ __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_con
         O += so[(w * 16 + h) * kOStride + d] * f;
       }
     }
-    if (single) {
-      const size_t oi = ((size_t)b * Hq + (size_t)hkv * G + h);
-      const float val = Ls > 0.f ? O / Ls : 0.f;
-      a.out[oi * kHeadDim + d] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
-      if (a.lse && d == 0) a.lse[oi] = (Ls > 0.f) ? (M + fast_log2(Ls)) * kLn2 : -INFINITY;
-    } else {
-      const size_t pi = ((size_t)bh * a.n_splits + split) * G + h;
-      a.part_o[pi * kHeadDim + d] = O;
-      if (d == 0) a.part_ml[pi] = make_float2(M, Ls);
+    octa[h * kHeadDim + d] = O;
+    if (d == 0) {
+      cta_m[h] = M;
+      cta_l[h] = Ls;
     }
   }
-  if (single) return;
-
-  __threadfence();
   __syncthreads();
-  if (tid == 0) s_last = atomicAdd(a.counters + bh, 1u) == (unsigned)(a.n_splits - 1);
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
 
-  for (int h = 0; h < G; ++h) {
-    const size_t p0 = (size_t)bh * a.n_splits * G + h;
+  if (MODE == kAttendSparse) trace_mark(a.err, kTrAttCtaMerged, false);
+  // ---- merge the CTAs of the cluster through distributed shared memory ----
+  const int CS = a.cluster, NC = a.n_splits / a.cluster;
+  const uint32_t rank = cluster_ctarank();
+  const int q = split / CS;
+  const int cols = kHeadDim / CS, c0 = (int)rank * cols;
+  cluster_sync();
+  const uint32_t am = smem_u32(cta_m), al = smem_u32(cta_l), ao = smem_u32(octa);
+  // every rank's (max, sum) per head, fetched once, all loads in parallel
+  for (int e = tid; e < CS * G; e += kAttendThreads) {
+    const int rr = e / G, h = e % G;
+    rk_m[rr][h] = ld_dsmem(dsmem_addr(am + 4 * h, rr));
+    rk_l[rr][h] = ld_dsmem(dsmem_addr(al + 4 * h, rr));
+  }
+  __syncthreads();
+  for (int e = tid; e < G * cols; e += kAttendThreads) {
+    const int h = e / cols, col = c0 + e % cols;
+    float ov[16];
+#pragma unroll
+    for (int rr = 0; rr < 16; ++rr) ov[rr] = rr < CS ? ld_dsmem(dsmem_addr(ao + 4 * (h * kHeadDim + col), rr)) : 0.f;
     float M = -INFINITY;
-    for (int sp = 0; sp < a.n_splits; ++sp) M = fmaxf(M, __ldcg(a.part_ml + p0 + (size_t)sp * G).x);
+#pragma unroll
+    for (int rr = 0; rr < 16; ++rr)
+      if (rr < CS) M = fmaxf(M, rk_m[rr][h]);
     float Ls = 0.f, O = 0.f;
     if (M != -INFINITY) {
-      for (int sp = 0; sp < a.n_splits; ++sp) {
-        const float2 ml = __ldcg(a.part_ml + p0 + (size_t)sp * G);
+#pragma unroll
+      for (int rr = 0; rr < 16; ++rr) {
+        if (rr < CS) {
+          const float f = fast_exp2(rk_m[rr][h] - M);
+          Ls += rk_l[rr][h] * f;
+          O += ov[rr] * f;
+        }
+      }
+    }
+    const size_t oi = ((size_t)b * Hq + (size_t)hkv * G + h);
+    if (NC == 1) {
+      const float val = Ls > 0.f ? O / Ls : 0.f;
+      a.out[oi * kHeadDim + col] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
+      if (a.lse && col == 0) a.lse[oi] = (Ls > 0.f) ? (M + fast_log2(Ls)) * kLn2 : -INFINITY;
+    } else {
+      const size_t pi = ((size_t)bh * NC + q) * G + h;
+      a.part_o[pi * kHeadDim + col] = O;
+      if (rank == 0 && col == c0) a.part_ml[pi] = make_float2(M, Ls);
+    }
+  }
+  if (NC == 1) {
+    if (MODE == kAttendSparse) trace_mark(a.err, kTrAttClusterMerged, false);
+    cluster_sync();  // no CTA leaves while others still read its shared memory
+    if (MODE == kAttendSparse) trace_mark(a.err, kTrAttExit, false);
+    return;
+  }
+
+  // ---- several clusters per problem: the last one to finish merges ----
+  __threadfence();
+  cluster_sync();
+  if (rank == 0 && tid == 0) {
+    const int last = atomicAdd(a.counters + bh, 1u) == (unsigned)(NC - 1);
+    for (int rr = 0; rr < CS; ++rr) st_dsmem(dsmem_addr(smem_u32(&s_last), rr), last);
+  }
+  cluster_sync();
+  if (!s_last) return;
+  __threadfence();
+  for (int e = tid; e < G * cols; e += kAttendThreads) {
+    const int h = e / cols, col = c0 + e % cols;
+    const size_t p0 = (size_t)bh * NC * G + h;
+    float M = -INFINITY;
+    for (int qq = 0; qq < NC; ++qq) M = fmaxf(M, __ldcg(a.part_ml + p0 + (size_t)qq * G).x);
+    float Ls = 0.f, O = 0.f;
+    if (M != -INFINITY) {
+      for (int qq = 0; qq < NC; ++qq) {
+        const float2 ml = __ldcg(a.part_ml + p0 + (size_t)qq * G);
         const float f = fast_exp2(ml.x - M);
         Ls += ml.y * f;
-        O += __ldcg(a.part_o + (p0 + (size_t)sp * G) * kHeadDim + d) * f;
+        O += __ldcg(a.part_o + (p0 + (size_t)qq * G) * kHeadDim + col) * f;
       }
     }
     const size_t oi = ((size_t)b * Hq + (size_t)hkv * G + h);
     const float val = Ls > 0.f ? O / Ls : 0.f;
-    a.out[oi * kHeadDim + d] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
-    if (a.lse && d == 0) a.lse[oi] = (Ls > 0.f) ? (M + fast_log2(Ls)) * kLn2 : -INFINITY;
+    a.out[oi * kHeadDim + col] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
+    if (a.lse && col == 0) a.lse[oi] = (Ls > 0.f) ? (M + fast_log2(Ls)) * kLn2 : -INFINITY;
   }
-  if (tid == 0) a.counters[bh] = 0;
+  if (rank == 0 && tid == 0) a.counters[bh] = 0;  // ready for the next call
 }
 
-template <int MODE>
+template <int MODE, int STAGES>
+size_t smem_bytes() {
+  return (size_t)STAGES * kStage + 1024;
+}
+
+template <int MODE, int STAGES>
 cudaError_t launch_mode(const AttendArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s,
                         bool pdl) {
-  const size_t smem = kStages * kStage + 1024;
-  cudaError_t e = cudaFuncSetAttribute(attend_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const size_t smem = smem_bytes<MODE, STAGES>();
+  auto kern = attend_kernel<MODE, STAGES>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
+  if (a.cluster > 8) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_splits, a.batch * a.num_kv_heads, 1);
   cfg.blockDim = dim3(kAttendThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  attr[na].id = cudaLaunchAttributeClusterDimension;
+  attr[na].val.clusterDim.x = MODE == kAttendPageLse ? 1 : a.cluster;
+  attr[na].val.clusterDim.y = 1;
+  attr[na].val.clusterDim.z = 1;
+  ++na;
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, attend_kernel<MODE>, tk, tv, a);
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, kern, tk, tv, a);
 }
 
+// Largest cluster size (16, 8, ... 1) the device can place for this kernel.
+template <int MODE, int STAGES>
+int max_cluster_of() {
+  auto kern = attend_kernel<MODE, STAGES>;
+  const size_t smem = smem_bytes<MODE, STAGES>();
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 1;
+  for (int cs = 16; cs > 1; cs /= 2) {
+    if (cs > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+      continue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cs, 1, 1);
+    cfg.blockDim = dim3(kAttendThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0) return cs;
+    (void)cudaGetLastError();
+  }
+  return 1;
+}
+
+constexpr int kSparseStages = 3;
+constexpr int kDenseStages = 2;
+
 }  // namespace
+
+int attend_max_cluster(int mode) {
+  static int cache[2][64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 8;
+  const int m = mode == kAttendSparse ? 0 : 1;
+  if (cache[m][dev] == 0)
+    cache[m][dev] = mode == kAttendSparse ? max_cluster_of<kAttendSparse, kSparseStages>()
+                                          : max_cluster_of<kAttendDense, kDenseStages>();
+  return cache[m][dev];
+}
 
 cudaError_t launch_attend(const AttendArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, int mode,
                           cudaStream_t s, bool pdl) {
   switch (mode) {
-    case kAttendSparse: return launch_mode<kAttendSparse>(a, tk, tv, s, pdl);
-    case kAttendDense: return launch_mode<kAttendDense>(a, tk, tv, s, pdl);
-    default: return launch_mode<kAttendPageLse>(a, tk, tv, s, pdl);
+    case kAttendSparse: return launch_mode<kAttendSparse, kSparseStages>(a, tk, tv, s, pdl);
+    case kAttendDense: return launch_mode<kAttendDense, kDenseStages>(a, tk, tv, s, pdl);
+    default: return launch_mode<kAttendPageLse, kDenseStages>(a, tk, tv, s, pdl);
   }
 }
 

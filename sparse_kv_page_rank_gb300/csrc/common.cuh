@@ -113,10 +113,24 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                "r"(bytes)
                : "memory");
 }
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
+}
+// Non-blocking test: has phase `parity` completed?
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
 // Wait for phase `parity` to complete; false after kMbarSpinLimit polls.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* polls = nullptr) {
   uint32_t addr = smem_u32(bar);
   for (uint32_t it = 0; it < kMbarSpinLimit; ++it) {
+    if (polls) ++*polls;
     uint32_t done;
     asm volatile(
         "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, "
@@ -139,8 +153,137 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
+// 1-D bulk copy global -> shared (both 16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(smem_dst),
+      "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_2d_u32(uint32_t smem_dst, const CUtensorMap* map, uint64_t* bar, int x,
+                                                int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%2, %3}], [%4];\n" ::"r"(smem_dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(v) : "r"(addr));
+  return v;
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ---- per-thread asynchronous global -> shared copies (LDGSTS) -------------------
+__device__ __forceinline__ void cp_async_16(uint32_t smem_addr, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_addr), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_4(uint32_t smem_addr, const void* gmem) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(smem_addr), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+// ---- thread-block clusters / distributed shared memory ------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+  return r;
+}
+// Hardware barrier over every CTA of the cluster (all CTAs of a cluster are
+// co-scheduled, so it always completes); release/acquire orders shared and
+// global memory accesses around it.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t dsmem_addr(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float ld_dsmem(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];\n" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_dsmem(uint32_t addr, int v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;\n" ::"r"(addr), "r"(v) : "memory");
+}
+
+// ---- optional kernel timeline (build with -DLOCKS_TRACE=1) -------------------------
+// Each kernel records %globaltimer (ns) at its first CTA entry, first return
+// from the grid-dependency wait, phase ends and last CTA exit, plus summed
+// per-warp cycle counts, into 64-bit slots that live in otherwise unused
+// bytes of the workspace's first 256-byte block (offset 8, 31 slots).  Start
+// slots must be preset to ~0 and the others to 0 by the reader.  Compiled out
+// by default.
+#ifndef LOCKS_TRACE
+#define LOCKS_TRACE 0
+#endif
+enum TraceSlot {
+  kTrScanEnter = 0, kTrScanWait, kTrScanExit,
+  kTrTopkEnter, kTrTopkWait, kTrTopkExit,
+  kTrAttEnter, kTrAttWait, kTrAttExit,
+  kTrScanCycWait, kTrScanCycCompute, kTrScanCycIssue, kTrScanPages,
+  kTrTopkLoaded, kTrTopkKeys, kTrTopkSelected,
+  kTrAttResolved, kTrAttFirstData, kTrAttLooped, kTrAttCtaMerged, kTrAttClusterMerged,
+  kTrScanPolls, kTrSelMinMax, kTrSelRadix, kTrSelCompact, kTrSelPasses, kTrSelCalls,
+  kTrScanLastEnter, kTrScanMaxDur, kTrScanLoopDone,
+};
+__device__ __forceinline__ unsigned long long trace_ns() {
+#if LOCKS_TRACE
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+#else
+  return 0ull;
+#endif
+}
+__device__ __forceinline__ void trace_max(int* err_word, int slot, unsigned long long v) {
+#if LOCKS_TRACE
+  if (err_word) atomicMax(reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(err_word) + 8) + slot, v);
+#else
+  (void)err_word; (void)slot; (void)v;
+#endif
+}
+__device__ __forceinline__ unsigned long long trace_clock() {
+#if LOCKS_TRACE
+  return clock64();
+#else
+  return 0ull;
+#endif
+}
+__device__ __forceinline__ void trace_add(int* err_word, int slot, unsigned long long v) {
+#if LOCKS_TRACE
+  if (err_word) atomicAdd(reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(err_word) + 8) + slot, v);
+#else
+  (void)err_word; (void)slot; (void)v;
+#endif
+}
+__device__ __forceinline__ void trace_mark(int* err_word, int slot, bool is_min) {
+#if LOCKS_TRACE
+  if (err_word && threadIdx.x == 0) {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    unsigned long long* tr = reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(err_word) + 8);
+    if (is_min) atomicMin(tr + slot, t); else atomicMax(tr + slot, t);
+  }
+#else
+  (void)err_word; (void)slot; (void)is_min;
+#endif
 }
 
 // ---- warp / block reductions ---------------------------------------------------

@@ -59,7 +59,10 @@ struct AttendArgs {
   float2* part_ml;            // ws: [B*Hkv][n_splits][G]
   unsigned* counters;         // ws: [B*Hkv]
   int* err;
-  int batch, num_kv_heads, group, max_pages, pages_total, k_max, n_splits;
+  int batch, num_kv_heads, group, max_pages, pages_total, k_max;
+  int n_splits;               // CTAs per problem = cluster * clusters per problem
+  int cluster;                // CTAs per thread-block cluster (1 in page-LSE mode)
+  int inputs_early;           // 1: the step's inputs may be read before the grid dependency wait
   float scale_log2;
 };
 
@@ -82,9 +85,13 @@ cudaError_t launch_attend(const AttendArgs& a, const CUtensorMap& tk, const CUte
 cudaError_t launch_build(const BuildArgs& a, cudaStream_t s);
 
 size_t topk_smem_bytes(size_t keys);
-constexpr int kScanThreads = 256;
-constexpr int kScanWarps = kScanThreads / 32;
-constexpr int kTopkThreads = 256;
+int topk_pages_per_cta(int group);  // pages one top-k CTA scores
+int attend_max_cluster(int mode);  // largest placeable cluster (<= 16) for that mode
+// Scan CTA: 7 consumer warps + 1 producer warp, so that two CTAs put four
+// warps on each SM sub-partition (whose register file is a quarter of the SM's).
+constexpr int kScanWarps = 7;
+constexpr int kScanThreads = (kScanWarps + 1) * 32;
+constexpr int kTopkThreads = 512;
 constexpr int kAttendThreads = 128;
 
 }  // namespace locks

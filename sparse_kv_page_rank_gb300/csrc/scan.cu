@@ -7,25 +7,34 @@
 // the coefficients and take their log-sum-exp (LOCKS abstract: "reconstructs
 // within-page logits, estimates each page's attention mass by log-sum-exp").
 // The summaries are "scanned in full each step" (abstract): this kernel is the
-// dominant byte stream of the decode step.
+// dominant byte stream of the decode step, so it is built to keep HBM busy.
 //
-// One warp handles one page-head at a time, for all G <= 16 heads of its
-// group at once, with two bf16 tensor-core contractions:
+// Memory (warp-specialised): each CTA owns a contiguous range of pages of one
+// (sequence, KV head) and a ring of S page-head slots in shared memory.  One
+// producer warp keeps the ring full: each of its lanes owns slots, waits for
+// the slot to be released, and issues two TMA bulk copies (the basis block,
+// r rows of 256 bytes, and the coefficient block, P x r), completing on the
+// slot's "full" mbarrier.  Seven consumer warps only compute: consumer w takes
+// pages w, w + 7, ..., waits on the slot's full barrier and releases it on its
+// "empty" barrier.  Up to S page-heads (96 KiB) per CTA are in flight,
+// independent of how long the consumers take per page.
+//
+// Compute: one consumer warp per page-head, all G <= 16 heads of the group at
+// once, two bf16 tensor-core contractions:
 //   (1) W^T = Q V_j        m16n8k16, M = heads, N = basis vectors, K = d.
-//       The contraction index d is permuted so that each lane's 16-byte load
+//       The contraction index d is permuted so that each lane's 16-byte piece
 //       of a basis row (d = 32s+8c .. +8) is exactly its B fragment for two
 //       k-steps; the query A fragments use the same permutation.  bf16 x bf16
 //       products are exact in the fp32 accumulator.
-//   (2) L^T = W^T C_j^T    m16n8k8 (r <= 8) or m16n8k16 (r = 16), M = heads,
+//   (2) L^T = W^T C_j^T    m16n8k8 (r <= 8) or m16n8k16 (r > 8), M = heads,
 //       N = tokens, K = r.  The fp32 W is split into three bf16 terms
-//       (hi + mid + lo, 24 bits) so the second product keeps fp32 accuracy.
-//       The accumulator of (1) is already in the A-fragment layout of (2), and
-//       token n-tile jt, column g is token 8*jt + g, so each coefficient load
-//       is one 4-byte word per lane and 128 contiguous bytes per warp.
-// Then a base-2 log-sum-exp over the 64 tokens per head (two xor-shuffles
-// across the four lanes of a row).  Each CTA also reduces its pages' s_hat
-// into a per-head (max, sum) pair, from which the top-k kernel gets the total
-// estimated mass Z_h of each head without re-reading every s_hat.
+//       (hi + mid + lo) so the second product keeps fp32 accuracy.  The
+//       accumulator of (1) is already in the A-fragment layout of (2);
+//       n-tile jt, column g is token 8*jt + g.
+// Then a base-2 log-sum-exp over the 64 tokens per head.  Each CTA also
+// reduces its pages' s_hat into a per-head (max, sum) pair, from which the
+// top-k kernel gets the total estimated mass Z_h of each head without
+// re-reading every s_hat.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -33,235 +42,381 @@ namespace locks {
 
 namespace {
 
-struct PageData {
-  uint4 bv[4];      // basis row g:   d = 32s + 8c .. +8, s = 0..3
-  uint4 bw[4];      // basis row g+8  (r > 8 only)
-  uint32_t cb[8];   // coefficients (2c, 2c+1) of token 8*jt + g
-  uint32_t cc[8];   // coefficients (2c+8, 2c+9) of token 8*jt + g (r > 8 only)
+template <bool R16>
+struct Ring {
+  static constexpr int kSlots = R16 ? 16 : 32;     // page-heads in flight per CTA
+  static constexpr int kCoef = R16 ? 4096 : 2048;  // basis block (r rows x 256 B) comes first
+  static constexpr int kSlot = R16 ? 6144 : 3072;
 };
 
 template <bool R16>
-__device__ __forceinline__ void load_page(PageData& p, const uint16_t* bas, const uint16_t* coe, int g,
-                                          int c, int r) {
-  const uint4 z4 = make_uint4(0, 0, 0, 0);
-#pragma unroll
-  for (int s = 0; s < 4; ++s)
-    p.bv[s] = (g < r) ? __ldg(reinterpret_cast<const uint4*>(bas + g * kHeadDim + 32 * s + 8 * c)) : z4;
-  if (R16) {
-#pragma unroll
-    for (int s = 0; s < 4; ++s)
-      p.bw[s] = (g + 8 < r)
-                    ? __ldg(reinterpret_cast<const uint4*>(bas + (g + 8) * kHeadDim + 32 * s + 8 * c))
-                    : z4;
-  }
-#pragma unroll
-  for (int jt = 0; jt < 8; ++jt)
-    p.cb[jt] = (2 * c < r) ? __ldg(reinterpret_cast<const uint32_t*>(coe + (8 * jt + g) * r + 2 * c)) : 0u;
-  if (R16) {
-#pragma unroll
-    for (int jt = 0; jt < 8; ++jt)
-      p.cc[jt] =
-          (2 * c + 8 < r) ? __ldg(reinterpret_cast<const uint32_t*>(coe + (8 * jt + g) * r + 2 * c + 8)) : 0u;
-  }
+constexpr int scan_smem_bytes() {
+  return Ring<R16>::kSlots * Ring<R16>::kSlot + 1024;
 }
 
-// x -> hi + mid + lo with each term a bf16; returned as packed pairs for (x0, x1).
+// x -> hi + mid + lo, each term a bf16 (truncated; the three keep about 21
+// bits of x), returned as packed pairs for (x0, x1), x0 in the low half.
 __device__ __forceinline__ void split3(float x0, float x1, uint32_t& hi, uint32_t& mid, uint32_t& lo) {
-  float h0 = bf16_round(x0), h1 = bf16_round(x1);
-  float r0 = x0 - h0, r1 = x1 - h1;
-  float m0 = bf16_round(r0), m1 = bf16_round(r1);
-  hi = pack_bf16(h0, h1);
-  mid = pack_bf16(m0, m1);
-  lo = pack_bf16(r0 - m0, r1 - m1);
+  const uint32_t u0 = __float_as_uint(x0) & 0xffff0000u, u1 = __float_as_uint(x1) & 0xffff0000u;
+  const float r0 = x0 - __uint_as_float(u0), r1 = x1 - __uint_as_float(u1);
+  const uint32_t v0 = __float_as_uint(r0) & 0xffff0000u, v1 = __float_as_uint(r1) & 0xffff0000u;
+  const float t0 = r0 - __uint_as_float(v0), t1 = r1 - __uint_as_float(v1);
+  hi = __byte_perm(u0, u1, 0x7632);
+  mid = __byte_perm(v0, v1, 0x7632);
+  lo = __byte_perm(__float_as_uint(t0), __float_as_uint(t1), 0x7632);
 }
 
-template <bool G16, bool R16>
+template <int N>
+__device__ __forceinline__ float tree_max(const float* v) {
+  if constexpr (N == 1) {
+    return v[0];
+  } else {
+    return fmaxf(tree_max<N / 2>(v), tree_max<N / 2>(v + N / 2));
+  }
+}
+template <int N>
+__device__ __forceinline__ float tree_sum(const float* v) {
+  if constexpr (N == 1) {
+    return v[0];
+  } else {
+    return tree_sum<N / 2>(v) + tree_sum<N / 2>(v + N / 2);
+  }
+}
+
+// Base-2 log-sum-exp of N values per lane over the lanes of one head (the
+// xor masks name the lanes sharing the head; 0 = unused).  When every lane's
+// values lie in (-100, 120), 2^v neither overflows nor loses the page's
+// mass, and the shared maximum is skipped.
+template <int N, int X0, int X1, int X2>
+__device__ __forceinline__ float lse2_lanes(float* v) {
+  float mx = tree_max<N>(v);
+  const bool direct = __all_sync(0xffffffffu, mx > -100.f && mx < 120.f);
+  if (!direct) {
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, X0));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, X1));
+    if (X2) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, X2));
+  } else {
+    mx = 0.f;
+  }
+#pragma unroll
+  for (int e = 0; e < N; ++e) v[e] = fast_exp2(v[e] - mx);
+  float sm = tree_sum<N>(v);
+  sm += __shfl_xor_sync(0xffffffffu, sm, X0);
+  sm += __shfl_xor_sync(0xffffffffu, sm, X1);
+  if (X2) sm += __shfl_xor_sync(0xffffffffu, sm, X2);
+  return mx + fast_log2(sm);
+}
+
+// G16: more than 8 heads in the group (both row halves of the MMA tiles).
+// R16: rank above 8 (two basis n-tiles, k16 second contraction).
+// GRP2: at most 4 heads and rank <= 8: the second contraction packs two
+// 32-token groups into one m16n8k16 (rows 0-3 use k 0-7 = coefficients of
+// tokens 16jt+n, rows 4-7 use k 8-15 = coefficients of tokens 16jt+8+n),
+// which halves its MMAs, exponentials and reductions.
+//
+// Page-head in shared memory at `slot` -> base-2 LSE for head g (e0) and,
+// with G16, head g + 8 (e1).
+template <bool G16, bool R16, bool GRP2>
+__device__ __forceinline__ void compute_page(uint32_t slot, const uint4 (&qa)[4], const uint4 (&qb)[4], int r,
+                                             float scale_log2, int lane, float& e0, float& e1) {
+  using RG = Ring<R16>;
+  const int g = lane >> 2, c = lane & 3;
+  const uint4 z4 = make_uint4(0, 0, 0, 0);
+  // basis row `row`, 16-byte piece d = 32*s + 8c (linear rows of 256 B)
+  auto basis_piece = [&](int row, int s) -> uint32_t { return slot + row * 256 + s * 64 + c * 16; };
+  auto coef_word = [&](int jt, int k0) -> uint32_t {
+    return slot + RG::kCoef + (uint32_t)(((8 * jt + g) * r + k0) * 2);
+  };
+
+  // (1) W^T = Q V  (16 heads x 8 or 16 basis vectors); two accumulators per
+  // n-tile halve the dependent MMA chain
+  float w0[4] = {0.f, 0.f, 0.f, 0.f}, w1[4] = {0.f, 0.f, 0.f, 0.f};
+  float x0[4] = {0.f, 0.f, 0.f, 0.f}, x1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    const uint4 bv = (g < r) ? lds128(basis_piece(g, s)) : z4;
+    mma_16816(w0, qa[s].x, qb[s].x, qa[s].y, qb[s].y, bv.x, bv.y);
+    mma_16816(x0, qa[s].z, qb[s].z, qa[s].w, qb[s].w, bv.z, bv.w);
+    if (R16) {
+      const uint4 bw = (g + 8 < r) ? lds128(basis_piece(g + 8, s)) : z4;
+      mma_16816(w1, qa[s].x, qb[s].x, qa[s].y, qb[s].y, bw.x, bw.y);
+      mma_16816(x1, qa[s].z, qb[s].z, qa[s].w, qb[s].w, bw.z, bw.w);
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    w0[e] += x0[e];
+    if (R16) w1[e] += x1[e];
+  }
+
+  if (GRP2) {
+    // rows g < 4 hold heads 0-3 in the k 0-7 half of the A fragment, rows
+    // 4-7 the same heads (repeated Q rows) in the k 8-15 half
+    uint32_t hh, mm, ll;
+    split3(w0[0] * scale_log2, w0[1] * scale_log2, hh, mm, ll);
+    const bool lo_half = lane < 16;
+    const uint32_t ha0 = lo_half ? hh : 0u, ha2 = lo_half ? 0u : hh;
+    const uint32_t ma0 = lo_half ? mm : 0u, ma2 = lo_half ? 0u : mm;
+    const uint32_t la0 = lo_half ? ll : 0u, la2 = lo_half ? 0u : ll;
+    uint32_t cbv[8];
+#pragma unroll
+    for (int jt = 0; jt < 8; ++jt) cbv[jt] = (2 * c < r) ? lds32(coef_word(jt, 2 * c)) : 0u;
+    float d[4][4];
+#pragma unroll
+    for (int jt = 0; jt < 4; ++jt) {
+      d[jt][0] = d[jt][1] = d[jt][2] = d[jt][3] = 0.f;
+      mma_16816(d[jt], la0, 0u, la2, 0u, cbv[2 * jt], cbv[2 * jt + 1]);
+      mma_16816(d[jt], ma0, 0u, ma2, 0u, cbv[2 * jt], cbv[2 * jt + 1]);
+      mma_16816(d[jt], ha0, 0u, ha2, 0u, cbv[2 * jt], cbv[2 * jt + 1]);
+    }
+    float v[8] = {d[0][0], d[0][1], d[1][0], d[1][1], d[2][0], d[2][1], d[3][0], d[3][1]};
+    e0 = lse2_lanes<8, 1, 2, 16>(v);
+    e1 = 0.f;
+    return;
+  }
+
+  // fold scale * log2(e), split into three bf16 terms
+  uint32_t h0, m0, l0, h1, m1, l1, h2 = 0, m2 = 0, l2 = 0, h3 = 0, m3 = 0, l3 = 0;
+  split3(w0[0] * scale_log2, w0[1] * scale_log2, h0, m0, l0);
+  split3(w0[2] * scale_log2, w0[3] * scale_log2, h1, m1, l1);
+  if (R16) {
+    split3(w1[0] * scale_log2, w1[1] * scale_log2, h2, m2, l2);
+    split3(w1[2] * scale_log2, w1[3] * scale_log2, h3, m3, l3);
+  }
+  uint32_t cb[8], cc[8];
+#pragma unroll
+  for (int jt = 0; jt < 8; ++jt) {
+    cb[jt] = (2 * c < r) ? lds32(coef_word(jt, 2 * c)) : 0u;
+    cc[jt] = (R16 && 2 * c + 8 < r) ? lds32(coef_word(jt, 2 * c + 8)) : 0u;
+  }
+  // (2) logits (base-2) for 16 heads x 64 tokens
+  float d[8][4];
+#pragma unroll
+  for (int jt = 0; jt < 8; ++jt) {
+    d[jt][0] = d[jt][1] = d[jt][2] = d[jt][3] = 0.f;
+    if (R16) {
+      mma_16816(d[jt], l0, l1, l2, l3, cb[jt], cc[jt]);
+      mma_16816(d[jt], m0, m1, m2, m3, cb[jt], cc[jt]);
+      mma_16816(d[jt], h0, h1, h2, h3, cb[jt], cc[jt]);
+    } else {
+      mma_1688(d[jt], l0, l1, cb[jt]);
+      mma_1688(d[jt], m0, m1, cb[jt]);
+      mma_1688(d[jt], h0, h1, cb[jt]);
+    }
+  }
+  // base-2 log-sum-exp over the 64 tokens of each head row (16 values per
+  // lane, four lanes per row)
+  float v[16];
+#pragma unroll
+  for (int jt = 0; jt < 8; ++jt) {
+    v[2 * jt] = d[jt][0];
+    v[2 * jt + 1] = d[jt][1];
+  }
+  e0 = lse2_lanes<16, 1, 2, 0>(v);
+  e1 = 0.f;
+  if (G16) {
+#pragma unroll
+    for (int jt = 0; jt < 8; ++jt) {
+      v[2 * jt] = d[jt][2];
+      v[2 * jt + 1] = d[jt][3];
+    }
+    e1 = lse2_lanes<16, 1, 2, 0>(v);
+  }
+}
+
+template <bool G16, bool R16, bool GRP2>
 __global__ void __launch_bounds__(kScanThreads, 2) scan_kernel(const ScanArgs a) {
+  using RG = Ring<R16>;
+  constexpr int S = RG::kSlots;
+  extern __shared__ uint8_t ring_raw[];
   __shared__ float2 red[kScanWarps][16];
+  __shared__ __align__(8) uint64_t full_bar[S], empty_bar[S];
+  __shared__ int slot_ok[S];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
   const int bh = blockIdx.y, chunk = blockIdx.x;
   const int b = bh / a.num_kv_heads, hkv = bh % a.num_kv_heads;
   const int G = a.group, r = a.rank;
+  const uint32_t ring = (smem_u32(ring_raw) + 1023u) & ~1023u;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
 
+  trace_mark(a.err, kTrScanEnter, true);
+  trace_mark(a.err, kTrScanLastEnter, false);
+  const unsigned long long t_enter = trace_ns();
   pdl_wait();
+  trace_mark(a.err, kTrScanWait, true);
 
   const int L = a.seq_lens[b];
   int ns = a.n_summarized[b];
   const int nfull = L < 0 ? 0 : L / kPage;
-  int cap = nfull < a.max_pages ? nfull : a.max_pages;
+  const int cap = nfull < a.max_pages ? nfull : a.max_pages;
   if (ns > cap || ns < 0 || L > a.max_pages * kPage) {
     if (threadIdx.x == 0 && chunk == 0) set_error(a.err, LOCKS_DEVERR_LENGTHS);
     ns = ns < 0 ? 0 : (ns > cap ? cap : ns);
   }
   const int j0 = chunk * a.chunk_pages;
   const int j1 = min(j0 + a.chunk_pages, ns);
-
-  // Query A fragments with the permuted contraction index.
-  const int Hq = a.num_kv_heads * G;
-  uint4 qa[4], qb[4];
-  {
-    const uint16_t* qrow = a.q + ((size_t)b * Hq + (size_t)hkv * G) * kHeadDim;
-#pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      qa[s] = (g < G) ? __ldg(reinterpret_cast<const uint4*>(qrow + g * kHeadDim + 32 * s + 8 * c))
-                      : make_uint4(0, 0, 0, 0);
-      qb[s] = (G16 && g + 8 < G)
-                  ? __ldg(reinterpret_cast<const uint4*>(qrow + (g + 8) * kHeadDim + 32 * s + 8 * c))
-                  : make_uint4(0, 0, 0, 0);
-    }
-  }
-
-  const size_t ph_stride_b = (size_t)r * kHeadDim;  // elements per page-head of basis
-  const size_t ph_stride_c = (size_t)kPage * r;     // elements per page-head of coeffs
-  const int32_t* bt = a.block_table + (size_t)b * a.max_pages;
+  const int n = j1 > j0 ? j1 - j0 : 0;  // pages of this CTA
 
   float zm0 = -INFINITY, zl0 = 0.f, zm1 = -INFINITY, zl1 = 0.f;
-
-  PageData cur, nxt;
-  int j = j0 + warp;
-  bool have = j < j1;
-  bool ok_cur = false;
-  if (have) {
-    int phys = bt[j];
-    ok_cur = phys >= 0 && phys < a.pages_total;
-    if (!ok_cur) { if (lane == 0) set_error(a.err, LOCKS_DEVERR_BLOCK_TABLE); phys = 0; }
-    size_t ph = (size_t)phys * a.num_kv_heads + hkv;
-    load_page<R16>(cur, a.basis_t + ph * ph_stride_b, a.coeffs + ph * ph_stride_c, g, c, r);
-  }
-  while (have) {
-    const int jn = j + kScanWarps;
-    const bool have_n = jn < j1;
-    bool ok_n = false;
-    if (have_n) {
-      int phys = bt[jn];
-      ok_n = phys >= 0 && phys < a.pages_total;
-      if (!ok_n) { if (lane == 0) set_error(a.err, LOCKS_DEVERR_BLOCK_TABLE); phys = 0; }
-      size_t ph = (size_t)phys * a.num_kv_heads + hkv;
-      load_page<R16>(nxt, a.basis_t + ph * ph_stride_b, a.coeffs + ph * ph_stride_c, g, c, r);
+  if (warp == kScanWarps) {
+    // ---- producer: lane l owns slot l (l < S) and fills pages l, l + S, ...
+    // Each lane tests its own slot without blocking, so a released slot is
+    // refilled at once whatever the other lanes' slots are doing.
+    const int32_t* bt = a.block_table + (size_t)b * a.max_pages;
+    const size_t ph_stride_b = (size_t)r * kHeadDim, ph_stride_c = (size_t)kPage * r;
+    const uint32_t basis_bytes = (uint32_t)(r * kHeadDim * 2), coef_bytes = (uint32_t)(kPage * r * 2);
+    // the block-table entries of this lane's first kPre pages, read up front
+    constexpr int kPre = 8;
+    int pre[kPre];
+#pragma unroll
+    for (int u = 0; u < kPre; ++u) pre[u] = (lane < S && lane + u * S < n) ? bt[j0 + lane + u * S] : -1;
+    int p = lane < S ? lane : n;  // next page of this lane
+    for (uint32_t spin = 0; __any_sync(0xffffffffu, p < n); ++spin) {
+      if (spin == kMbarSpinLimit * 4u) {
+        if (lane == 0) set_error(a.err, kDevErrTimeout);
+        break;
+      }
+      const bool ready = p < n && (p < S || mbar_test(&empty_bar[lane], (uint32_t)(((p / S) - 1) & 1)));
+      if (!__any_sync(0xffffffffu, ready)) {
+        __nanosleep(64);
+        continue;
+      }
+      if (ready) {
+        const int u = p / S;
+        int phys = -1;
+#pragma unroll
+        for (int v = 0; v < kPre; ++v)
+          if (v == u) phys = pre[v];
+        if (u >= kPre) phys = bt[j0 + p];
+        const bool valid = phys >= 0 && phys < a.pages_total;
+        slot_ok[lane] = valid ? 1 : 0;
+        if (valid) {
+          const size_t ph = (size_t)phys * a.num_kv_heads + hkv;
+          const uint32_t slot = ring + lane * RG::kSlot;
+          mbar_arrive_expect_tx(&full_bar[lane], basis_bytes + coef_bytes);
+          bulk_load(slot, a.basis_t + ph * ph_stride_b, basis_bytes, &full_bar[lane]);
+          bulk_load(slot + RG::kCoef, a.coeffs + ph * ph_stride_c, coef_bytes, &full_bar[lane]);
+        } else {
+          mbar_arrive(&full_bar[lane]);
+        }
+        p += S;
+      }
     }
-
-    if (ok_cur) {
-      // (1) W^T = Q V  (16 heads x 8 or 16 basis vectors)
-      float w0[4] = {0.f, 0.f, 0.f, 0.f}, w1[4] = {0.f, 0.f, 0.f, 0.f};
+  } else {
+    // ---- consumers
+    const int Hq = a.num_kv_heads * G;
+    uint4 qa[4], qb[4];
+    {
+      // query A fragments with the permuted contraction index; GRP2: rows
+      // 4-7 repeat heads 0-3, so the first contraction already leaves each
+      // head's W in both row halves the second one needs
+      const uint16_t* qrow = a.q + ((size_t)b * Hq + (size_t)hkv * G) * kHeadDim;
+      const int qr = GRP2 ? (g & 3) : g;
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
-        mma_16816(w0, qa[s].x, qb[s].x, qa[s].y, qb[s].y, cur.bv[s].x, cur.bv[s].y);
-        mma_16816(w0, qa[s].z, qb[s].z, qa[s].w, qb[s].w, cur.bv[s].z, cur.bv[s].w);
-        if (R16) {
-          mma_16816(w1, qa[s].x, qb[s].x, qa[s].y, qb[s].y, cur.bw[s].x, cur.bw[s].y);
-          mma_16816(w1, qa[s].z, qb[s].z, qa[s].w, qb[s].w, cur.bw[s].z, cur.bw[s].w);
-        }
+        qa[s] = (qr < G && (!GRP2 || g < 8))
+                    ? __ldg(reinterpret_cast<const uint4*>(qrow + qr * kHeadDim + 32 * s + 8 * c))
+                    : make_uint4(0, 0, 0, 0);
+        qb[s] = (G16 && g + 8 < G)
+                    ? __ldg(reinterpret_cast<const uint4*>(qrow + (g + 8) * kHeadDim + 32 * s + 8 * c))
+                    : make_uint4(0, 0, 0, 0);
       }
-      // fold scale * log2(e), split into three bf16 terms
-      uint32_t h0, m0, l0, h1, m1, l1, h2 = 0, m2 = 0, l2 = 0, h3 = 0, m3 = 0, l3 = 0;
-      split3(w0[0] * a.scale_log2, w0[1] * a.scale_log2, h0, m0, l0);
-      split3(w0[2] * a.scale_log2, w0[3] * a.scale_log2, h1, m1, l1);
-      if (R16) {
-        split3(w1[0] * a.scale_log2, w1[1] * a.scale_log2, h2, m2, l2);
-        split3(w1[2] * a.scale_log2, w1[3] * a.scale_log2, h3, m3, l3);
+    }
+    unsigned long long cyc_wait = 0, cyc_comp = 0;
+    for (int p = warp; p < n; p += kScanWarps) {
+      const int s = p % S;
+      const unsigned long long t0 = trace_clock();
+      const bool ok = mbar_wait(&full_bar[s], (uint32_t)((p / S) & 1));
+      const unsigned long long t1 = trace_clock();
+      if (__any_sync(0xffffffffu, !ok)) {
+        if (lane == 0) set_error(a.err, kDevErrTimeout);
+        break;
       }
-      // (2) logits (base-2) for 16 heads x 64 tokens
-      float d[8][4];
-#pragma unroll
-      for (int jt = 0; jt < 8; ++jt) {
-        d[jt][0] = d[jt][1] = d[jt][2] = d[jt][3] = 0.f;
-        if (R16) {
-          mma_16816(d[jt], l0, l1, l2, l3, cur.cb[jt], cur.cc[jt]);
-          mma_16816(d[jt], m0, m1, m2, m3, cur.cb[jt], cur.cc[jt]);
-          mma_16816(d[jt], h0, h1, h2, h3, cur.cb[jt], cur.cc[jt]);
-        } else {
-          mma_1688(d[jt], l0, l1, cur.cb[jt]);
-          mma_1688(d[jt], m0, m1, cur.cb[jt]);
-          mma_1688(d[jt], h0, h1, cur.cb[jt]);
-        }
+      const int valid = slot_ok[s];
+      float e0 = 0.f, e1 = 0.f;
+      if (valid) compute_page<G16, R16, GRP2>(ring + s * RG::kSlot, qa, qb, r, a.scale_log2, lane, e0, e1);
+      __syncwarp();  // every lane is done with the slot
+      if (lane == 0) mbar_arrive(&empty_bar[s]);
+      cyc_wait += t1 - t0;
+      cyc_comp += trace_clock() - t1;
+      if (!valid) {
+        if (lane == 0) set_error(a.err, LOCKS_DEVERR_BLOCK_TABLE);
+        continue;
       }
-      // base-2 log-sum-exp over the 64 tokens of each head row
-      float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-      for (int jt = 0; jt < 8; ++jt) {
-        mx0 = fmaxf(mx0, fmaxf(d[jt][0], d[jt][1]));
-        if (G16) mx1 = fmaxf(mx1, fmaxf(d[jt][2], d[jt][3]));
-      }
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-      if (G16) {
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-      }
-      float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-      for (int jt = 0; jt < 8; ++jt) {
-        s0 += fast_exp2(d[jt][0] - mx0) + fast_exp2(d[jt][1] - mx0);
-        if (G16) s1 += fast_exp2(d[jt][2] - mx1) + fast_exp2(d[jt][3] - mx1);
-      }
-      s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
-      s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
-      if (G16) {
-        s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
-        s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
-      }
-      const float e0 = mx0 + fast_log2(s0);
+      const int j = j0 + p;
       lse2_merge(zm0, zl0, e0, 1.f);
-      float e1 = 0.f;
-      if (G16) {
-        e1 = mx1 + fast_log2(s1);
-        lse2_merge(zm1, zl1, e1, 1.f);
-      }
+      if (G16) lse2_merge(zm1, zl1, e1, 1.f);
       if (c == 0) {
         float* dst = a.shat + ((size_t)bh * a.max_pages + j) * G;
-        if (g < G) dst[g] = e0 * kLn2;
+        if (g < G && (!GRP2 || g < 4)) dst[g] = e0 * kLn2;
         if (G16 && g + 8 < G) dst[g + 8] = e1 * kLn2;
         if (a.page_lse) {
           float* pl = a.page_lse + ((size_t)b * Hq + (size_t)hkv * G) * a.max_pages + j;
-          if (g < G) pl[(size_t)g * a.max_pages] = e0 * kLn2;
+          if (g < G && (!GRP2 || g < 4)) pl[(size_t)g * a.max_pages] = e0 * kLn2;
           if (G16 && g + 8 < G) pl[(size_t)(g + 8) * a.max_pages] = e1 * kLn2;
         }
       }
     }
-    cur = nxt;
-    ok_cur = ok_n;
-    j = jn;
-    have = have_n;
+    if (lane == 0) {
+      trace_add(a.err, kTrScanCycWait, cyc_wait);
+      trace_add(a.err, kTrScanCycCompute, cyc_comp);
+      trace_add(a.err, kTrScanPages, (unsigned long long)((n - warp + kScanWarps - 1) / kScanWarps));
+    }
+    if (c == 0 && (!GRP2 || g < 4)) {
+      red[warp][g] = make_float2(zm0, zl0);
+      if (G16) red[warp][g + 8] = make_float2(zm1, zl1);
+    }
   }
 
+  if (LOCKS_TRACE && lane == 0 && warp < kScanWarps) trace_mark(a.err, kTrScanLoopDone, false);
   pdl_launch_dependents();
-
-  if (c == 0) {
-    red[warp][g] = make_float2(zm0, zl0);
-    if (G16) red[warp][g + 8] = make_float2(zm1, zl1);
-  }
   __syncthreads();
+  if (threadIdx.x == 0) trace_max(a.err, kTrScanMaxDur, trace_ns() - t_enter);
   if (threadIdx.x < G) {
     float m = -INFINITY, l = 0.f;
 #pragma unroll
     for (int w = 0; w < kScanWarps; ++w) lse2_merge(m, l, red[w][threadIdx.x].x, red[w][threadIdx.x].y);
     a.part[((size_t)bh * a.n_chunks + chunk) * G + threadIdx.x] = make_float2(m, l);
   }
+  trace_mark(a.err, kTrScanExit, false);
 }
 
-template <bool G16, bool R16>
+template <bool G16, bool R16, bool GRP2>
 cudaError_t launch_one(const ScanArgs& a, cudaStream_t s, bool pdl) {
+  const int smem = scan_smem_bytes<R16>();
+  cudaError_t e =
+      cudaFuncSetAttribute(scan_kernel<G16, R16, GRP2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_chunks, a.batch * a.num_kv_heads, 1);
   cfg.blockDim = dim3(kScanThreads, 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, scan_kernel<G16, R16>, a);
+  return cudaLaunchKernelEx(&cfg, scan_kernel<G16, R16, GRP2>, a);
 }
 
 }  // namespace
 
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s, bool pdl) {
   const bool g16 = a.group > 8, r16 = a.rank > 8;
-  if (g16) return r16 ? launch_one<true, true>(a, s, pdl) : launch_one<true, false>(a, s, pdl);
-  return r16 ? launch_one<false, true>(a, s, pdl) : launch_one<false, false>(a, s, pdl);
+  if (g16) return r16 ? launch_one<true, true, false>(a, s, pdl) : launch_one<true, false, false>(a, s, pdl);
+  if (r16) return launch_one<false, true, false>(a, s, pdl);
+  if (a.group <= 4) return launch_one<false, false, true>(a, s, pdl);
+  return launch_one<false, false, false>(a, s, pdl);
 }
 
 }  // namespace locks

@@ -55,8 +55,10 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* sm_warp, int& to
 }
 
 struct SelectShared {
-  unsigned hist[256];
+  unsigned hist[kWarps][256];  // one row per warp: no atomics shared across warps
+  unsigned total[256];
   int warp_tmp[kWarps];
+  unsigned wmin[kWarps], wmax[kWarps];
   unsigned bucket;
   unsigned remaining;
 };
@@ -64,28 +66,74 @@ struct SelectShared {
 // Choose the k largest of keys[0..n) (ties -> lower position) and call
 // emit(position_in_output, i) for each chosen i, positions in array order.
 template <typename Emit>
-__device__ void block_select(const uint32_t* keys, int n, int k, SelectShared& sh, Emit emit) {
+__device__ void block_select(const uint32_t* keys, int n, int k, SelectShared& sh, Emit emit,
+                             int* select_trace_err = nullptr) {
   const int tid = threadIdx.x;
   if (k <= 0 || n <= 0) return;
   uint32_t T = 0;
   unsigned need_eq = 0;
   const bool take_all = k >= n;
+  unsigned long long tc0 = trace_clock(), tc1 = tc0, tc2 = tc0;
+  int npass = 0;
   if (!take_all) {
-    uint32_t prefix = 0, mask = 0;
+    // only the bits below the highest bit where the keys differ need radix
+    // passes: the keys' range [min, max] fixes the others
+    unsigned lo = 0xffffffffu, hi = 0u;
+    for (int i = tid; i < n; i += kTopkThreads) {
+      const uint32_t key = keys[i];
+      lo = min(lo, key);
+      hi = max(hi, key);
+    }
+    lo = __reduce_min_sync(0xffffffffu, lo);
+    hi = __reduce_max_sync(0xffffffffu, hi);
+    if ((tid & 31) == 0) {
+      sh.wmin[tid >> 5] = lo;
+      sh.wmax[tid >> 5] = hi;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      lo = min(lo, sh.wmin[w]);
+      hi = max(hi, sh.wmax[w]);
+    }
+    const int nbits = (lo == hi) ? 0 : 32 - __clz(lo ^ hi);
+    const int passes = (nbits + 7) / 8;
+    npass = passes;
+    tc1 = trace_clock();
+    const uint32_t lowmask = passes >= 4 ? 0xffffffffu : ((1u << (8 * passes)) - 1u);
+    uint32_t prefix = lo & ~lowmask, mask = ~lowmask;
     unsigned rem = (unsigned)k;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      for (int i = tid; i < 256; i += kTopkThreads) sh.hist[i] = 0;
+    for (int shift = 8 * (passes - 1); shift >= 0; shift -= 8) {
+      for (int i = tid; i < kWarps * 256; i += kTopkThreads) (&sh.hist[0][0])[i] = 0;
       __syncthreads();
-      for (int i = tid; i < n; i += kTopkThreads) {
-        uint32_t key = keys[i];
-        if ((key & mask) == prefix) atomicAdd(&sh.hist[(key >> shift) & 255u], 1u);
+      // histogram of the next digit among keys matching the prefix so far
+      const int n_round = (n + kTopkThreads - 1) / kTopkThreads * kTopkThreads;
+      for (int i = tid; i < n_round; i += kTopkThreads) {
+        unsigned digit = 256u;
+        if (i < n) {
+          const uint32_t key = keys[i];
+          if ((key & mask) == prefix) digit = (key >> shift) & 255u;
+        }
+        // lanes agreeing with lane 0 (the common case) add once
+        const unsigned lead = __shfl_sync(0xffffffffu, digit, 0);
+        const unsigned same = __ballot_sync(0xffffffffu, digit == lead);
+        unsigned* row = sh.hist[threadIdx.x >> 5];
+        if ((threadIdx.x & 31) == 0 && lead < 256u) atomicAdd(&row[lead], __popc(same));
+        if (digit != lead && digit < 256u) atomicAdd(&row[digit], 1u);
+      }
+      __syncthreads();
+      for (int bin = tid; bin < 256; bin += kTopkThreads) {
+        unsigned t = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) t += sh.hist[w][bin];
+        sh.total[bin] = t;
       }
       __syncthreads();
       if (tid < 32) {
         // lane l owns buckets 8l .. 8l+7; count of keys in buckets above its range
         unsigned cnt[8], tot = 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) { cnt[i] = sh.hist[8 * tid + i]; tot += cnt[i]; }
+        for (int i = 0; i < 8; ++i) { cnt[i] = sh.total[8 * tid + i]; tot += cnt[i]; }
         unsigned incl = tot;  // sum over lanes >= tid
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -113,6 +161,7 @@ __device__ void block_select(const uint32_t* keys, int n, int k, SelectShared& s
     }
     T = prefix;
     need_eq = rem;
+    tc2 = trace_clock();
   }
   // blocked ranges in array order
   const int ipt = (n + kTopkThreads - 1) / kTopkThreads;
@@ -144,9 +193,23 @@ __device__ void block_select(const uint32_t* keys, int n, int k, SelectShared& s
       if (t) emit(pos++, i);
     }
   }
+  if (tid == 0) {
+    const unsigned long long tc3 = trace_clock();
+    trace_add(select_trace_err, kTrSelMinMax, tc1 - tc0);
+    trace_add(select_trace_err, kTrSelRadix, tc2 - tc1);
+    trace_add(select_trace_err, kTrSelCompact, tc3 - tc2);
+    trace_add(select_trace_err, kTrSelPasses, (unsigned long long)npass);
+    trace_add(select_trace_err, kTrSelCalls, 1ull);
+  }
 }
 
+// GT: heads per group (compile time; 0 = any G <= 16 at run time).
+// Each thread owns IPT consecutive pages of the chunk, whose s_hat rows it
+// loads together with the lengths and the scan partials in one round trip.
+template <int GT>
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs a) {
+  constexpr int GMAX = GT ? GT : 16;
+  constexpr int IPT = GT ? (32 / GT < 8 ? 32 / GT : 8) : 2;  // pages per thread
   extern __shared__ __align__(16) uint8_t dyn[];
   uint32_t* keys = reinterpret_cast<uint32_t*>(dyn);
   int32_t* idx = reinterpret_cast<int32_t*>(dyn + a.smem_keys * sizeof(uint32_t));
@@ -157,14 +220,59 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int chunk = blockIdx.x, bh = blockIdx.y;
   const int b = bh / a.num_kv_heads;
-  const int G = a.group;
+  const int G = GT ? GT : a.group;
 
+  trace_mark(a.err, kTrTopkEnter, true);
   pdl_wait();
+  trace_mark(a.err, kTrTopkWait, true);
+  // the attention kernel that follows may start its prologue now; it waits
+  // for this grid to finish before reading the selection
+  pdl_launch_dependents();
 
+  // ---- one round trip: lengths, scan partials (warp h: head h), s_hat rows
   const int L = a.seq_lens[b];
+  int ns = a.n_summarized[b];
+  float2 pv[4];
+  const float2* pbase = a.part + (size_t)bh * a.n_scan_chunks * G;
+  if (warp < G) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = lane + 32 * u;
+      pv[u] = i < a.n_scan_chunks ? __ldcg(pbase + (size_t)i * G + warp) : make_float2(-INFINITY, 0.f);
+    }
+  }
+  // pages j0 + tid + kTopkThreads * p: a warp reads consecutive rows
+  const int j0 = chunk * a.chunk_pages;
+  float sv[IPT][GMAX];
+  {
+    const float* sbase = a.shat + (size_t)bh * a.max_pages * G;
+#pragma unroll
+    for (int p = 0; p < IPT; ++p) {
+      const int j = j0 + tid + kTopkThreads * p;
+      const bool in = j < a.max_pages;
+      const float* row = sbase + (size_t)j * G;
+      if (GT != 0 && GT % 4 == 0) {
+#pragma unroll
+        for (int h4 = 0; h4 < GMAX / 4; ++h4) {
+          const float4 v = in ? __ldcg(reinterpret_cast<const float4*>(row) + h4) : make_float4(0.f, 0.f, 0.f, 0.f);
+          sv[p][4 * h4] = v.x;
+          sv[p][4 * h4 + 1] = v.y;
+          sv[p][4 * h4 + 2] = v.z;
+          sv[p][4 * h4 + 3] = v.w;
+        }
+      } else if (GT == 2) {
+        const float2 v = in ? __ldcg(reinterpret_cast<const float2*>(row)) : make_float2(0.f, 0.f);
+        sv[p][0] = v.x;
+        sv[p][GMAX > 1 ? 1 : 0] = v.y;
+      } else {
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h) sv[p][h] = (in && h < G) ? __ldcg(row + h) : 0.f;
+      }
+    }
+  }
+
   const int nfull = L < 0 ? 0 : L / kPage;
   const int cap = nfull < a.max_pages ? nfull : a.max_pages;
-  int ns = a.n_summarized[b];
   ns = ns < 0 ? 0 : (ns > cap ? cap : ns);
   const int k = ns < a.k_max ? ns : a.k_max;
   int32_t* sel = a.sel_pages + (size_t)bh * a.k_max;
@@ -175,57 +283,65 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs a) {
       for (int i = tid; i < ns; i += kTopkThreads) sel[i] = i;
       if (tid == 0) a.sel_count[bh] = ns;
     }
-    pdl_launch_dependents();
+    trace_mark(a.err, kTrTopkExit, false);
     return;
   }
 
-  // Z_h (natural log) from the scan partials
-  for (int h = warp; h < G; h += kWarps) {
+  // Z_h (natural log): the remaining partials, then a warp reduction
+  if (warp < G) {
     float m = -INFINITY, l = 0.f;
-    const float2* p = a.part + (size_t)bh * a.n_scan_chunks * G + h;
-    for (int i = lane; i < a.n_scan_chunks; i += 32) {
-      float2 v = __ldcg(p + (size_t)i * G);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) lse2_merge(m, l, pv[u].x, pv[u].y);
+    for (int i = lane + 128; i < a.n_scan_chunks; i += 32) {
+      const float2 v = __ldcg(pbase + (size_t)i * G + warp);
       lse2_merge(m, l, v.x, v.y);
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) {
-      float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-      float l2 = __shfl_xor_sync(0xffffffffu, l, o);
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+      const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
       lse2_merge(m, l, m2, l2);
     }
-    if (lane == 0) zsh[h] = (m + fast_log2(l)) * kLn2;
+    if (lane == 0) zsh[warp] = (m + fast_log2(l)) * kLn2;
   }
   __syncthreads();
+  trace_mark(a.err, kTrTopkLoaded, false);
 
-  const int j0 = chunk * a.chunk_pages;
+  // sigma_j = ln( (1/G) sum_h exp(s_hat[h][j] - Z_h) ) -> order-preserving keys
   const int j1 = min(j0 + a.chunk_pages, ns);
   const int nloc = j1 > j0 ? j1 - j0 : 0;
-  const float log2G = log2f((float)G);
-  for (int i = tid; i < nloc; i += kTopkThreads) {
-    const float* s = a.shat + ((size_t)bh * a.max_pages + j0 + i) * G;
-    float y[16];
-    float mx = -INFINITY;
+  {
+    const float log2G = log2f((float)G);
+    float zl[GMAX];
 #pragma unroll
-    for (int h = 0; h < 16; ++h) {
-      if (h < G) {
-        y[h] = (__ldcg(s + h) - zsh[h]) * kLog2e;
-        mx = fmaxf(mx, y[h]);
+    for (int h = 0; h < GMAX; ++h) zl[h] = h < G ? zsh[h] * kLog2e : 0.f;
+#pragma unroll
+    for (int p = 0; p < IPT; ++p) {
+      const int jl = tid + kTopkThreads * p;
+      if (jl < nloc) {
+        float y[GMAX];
+        float mx = -INFINITY;
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h) {
+          y[h] = h < G ? fmaf(sv[p][h], kLog2e, -zl[h]) : -INFINITY;
+          mx = fmaxf(mx, y[h]);
+        }
+        float acc = 0.f;
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h) acc += h < G ? fast_exp2(y[h] - mx) : 0.f;
+        keys[jl] = orderable_key((mx + fast_log2(acc) - log2G) * kLn2);
       }
     }
-    float acc = 0.f;
-#pragma unroll
-    for (int h = 0; h < 16; ++h)
-      if (h < G) acc += fast_exp2(y[h] - mx);
-    float sigma = (mx + fast_log2(acc) - log2G) * kLn2;
-    keys[i] = orderable_key(sigma);
   }
   __syncthreads();
+  trace_mark(a.err, kTrTopkKeys, false);
 
   const int kloc = k < nloc ? k : nloc;
   if (a.n_chunks == 1) {
-    block_select(keys, nloc, kloc, sh, [&](int pos, int i) { sel[pos] = j0 + i; });
+    block_select(keys, nloc, kloc, sh, [&](int pos, int i) { sel[pos] = j0 + i; }, a.err);
     if (tid == 0) a.sel_count[bh] = kloc;
-    pdl_launch_dependents();
+    trace_mark(a.err, kTrTopkSelected, false);
+    trace_mark(a.err, kTrTopkExit, false);
     return;
   }
 
@@ -247,16 +363,27 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs a) {
   __threadfence();
 
   // gather every chunk's candidates, in chunk (= page) order
-  int n_all = 0;
-  for (int ch = 0; ch < a.n_chunks; ++ch) {
-    const int cnt = __ldcg(a.cand_cnt + (size_t)bh * a.n_chunks + ch);
-    const uint32_t* sk = a.cand_key + ((size_t)bh * a.n_chunks + ch) * a.k_max;
-    const int32_t* si = a.cand_idx + ((size_t)bh * a.n_chunks + ch) * a.k_max;
-    for (int i = tid; i < cnt; i += kTopkThreads) {
-      keys[n_all + i] = __ldcg(sk + i);
-      idx[n_all + i] = __ldcg(si + i);
+  __shared__ int s_cnt[64];
+  __shared__ int s_off[65];
+  for (int ch = tid; ch < a.n_chunks; ch += kTopkThreads)
+    if (ch < 64) s_cnt[ch] = __ldcg(a.cand_cnt + (size_t)bh * a.n_chunks + ch);
+  __syncthreads();
+  if (tid == 0) {
+    int o = 0;
+    for (int ch = 0; ch < a.n_chunks && ch < 64; ++ch) {
+      s_off[ch] = o;
+      o += s_cnt[ch];
     }
-    n_all += cnt;
+    s_off[a.n_chunks < 64 ? a.n_chunks : 64] = o;
+  }
+  __syncthreads();
+  const int n_all = s_off[a.n_chunks < 64 ? a.n_chunks : 64];
+  for (int e = tid; e < a.n_chunks * a.k_max; e += kTopkThreads) {
+    const int ch = e / a.k_max, i = e % a.k_max;
+    if (ch < 64 && i < s_cnt[ch]) {
+      keys[s_off[ch] + i] = __ldcg(a.cand_key + ((size_t)bh * a.n_chunks + ch) * a.k_max + i);
+      idx[s_off[ch] + i] = __ldcg(a.cand_idx + ((size_t)bh * a.n_chunks + ch) * a.k_max + i);
+    }
   }
   __syncthreads();
   block_select(keys, n_all, k, sh, [&](int pos, int i) { sel[pos] = idx[i]; });
@@ -264,19 +391,20 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs a) {
     a.sel_count[bh] = k;
     a.counters[bh] = 0;  // ready for the next call
   }
-  pdl_launch_dependents();
+  trace_mark(a.err, kTrTopkExit, false);
 }
 
 }  // namespace
 
 size_t topk_smem_bytes(size_t keys) { return keys * (sizeof(uint32_t) + sizeof(int32_t)); }
 
-cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s, bool pdl) {
+namespace {
+
+template <int GT>
+cudaError_t launch_g(const TopkArgs& a, cudaStream_t s, bool pdl) {
   const size_t smem = topk_smem_bytes(a.smem_keys);
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-  }
+  cudaError_t e = cudaFuncSetAttribute(topk_kernel<GT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_chunks, a.batch * a.num_kv_heads, 1);
   cfg.blockDim = dim3(kTopkThreads, 1, 1);
@@ -287,7 +415,26 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s, bool pdl) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, topk_kernel, a);
+  return cudaLaunchKernelEx(&cfg, topk_kernel<GT>, a);
+}
+
+}  // namespace
+
+int topk_pages_per_cta(int group) {
+  const int gt = (group == 1 || group == 2 || group == 4 || group == 8 || group == 16) ? group : 0;
+  const int ipt = gt ? (32 / gt < 8 ? 32 / gt : 8) : 2;
+  return ipt * kTopkThreads;
+}
+
+cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s, bool pdl) {
+  switch (a.group) {
+    case 1: return launch_g<1>(a, s, pdl);
+    case 2: return launch_g<2>(a, s, pdl);
+    case 4: return launch_g<4>(a, s, pdl);
+    case 8: return launch_g<8>(a, s, pdl);
+    case 16: return launch_g<16>(a, s, pdl);
+    default: return launch_g<0>(a, s, pdl);
+  }
 }
 
 }  // namespace locks
