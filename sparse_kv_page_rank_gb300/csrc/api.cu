@@ -130,9 +130,9 @@ Plan make_plan(const locks_cache_t* c, const locks_params_t* p) {
       long long nc = target / (BH * csd);
       nc = std::max<long long>(1, std::min<long long>(nc, (c->max_pages + csd - 1) / csd));
       const long long ctas = BH * csd * nc;
-      // prefer large clusters (cheap on-chip merges) unless a smaller one
-      // fills the wave clearly better
-      if (ctas <= target && (best < 0 || ctas * 10 > best * 12)) {
+      // the fullest wave wins; among equals the larger cluster (cheaper
+      // on-chip merge), since the loop runs from large to small clusters
+      if (ctas <= target && ctas > best) {
         best = ctas;
         pl.dense_cluster = csd;
         pl.dense_nc = (int)nc;

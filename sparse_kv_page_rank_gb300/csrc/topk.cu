@@ -203,6 +203,135 @@ __device__ void block_select(const uint32_t* keys, int n, int k, SelectShared& s
   }
 }
 
+// Faster selection for the common case.  One histogram pass over the top 11
+// bits in which the keys differ (2048 bins) finds the bin that holds the k-th
+// largest key; keys in higher bins are all taken, and the few keys of that
+// boundary bin are ranked against each other (key descending, position
+// ascending) to take the rest.  When the boundary bin holds more than 256
+// keys (many equal or nearly equal keys) the radix select above is used.
+// Output order and ties are as in block_select.
+struct FastShared {
+  unsigned bins[2048];
+  uint32_t bkey[256];
+  int bidx[256];
+  int wsum[kWarps];
+  unsigned wmin[kWarps], wmax[kWarps];
+  int b_bin, b_above, b_cnt;
+};
+
+template <typename Emit>
+__device__ void fast_select(const uint32_t* keys, uint8_t* bflag, int n, int k, SelectShared& sh,
+                            FastShared& fs, Emit emit, int* select_trace_err = nullptr) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (k <= 0 || n <= 0) return;
+  if (k >= n) {
+    for (int i = tid; i < n; i += kTopkThreads) emit(i, i);
+    return;
+  }
+  const unsigned long long tc0 = trace_clock();
+  unsigned lo = 0xffffffffu, hi = 0u;
+  for (int i = tid; i < n; i += kTopkThreads) {
+    const uint32_t key = keys[i];
+    lo = min(lo, key);
+    hi = max(hi, key);
+  }
+  lo = __reduce_min_sync(0xffffffffu, lo);
+  hi = __reduce_max_sync(0xffffffffu, hi);
+  if (lane == 0) {
+    fs.wmin[warp] = lo;
+    fs.wmax[warp] = hi;
+  }
+  for (int b = tid; b < 2048; b += kTopkThreads) fs.bins[b] = 0;
+  if (tid == 0) fs.b_cnt = 0;
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    lo = min(lo, fs.wmin[w]);
+    hi = max(hi, fs.wmax[w]);
+  }
+  if (lo == hi) {  // all keys equal: the first k positions
+    for (int i = tid; i < k; i += kTopkThreads) emit(i, i);
+    return;
+  }
+  // bins: the top 11 of the bits in which the keys differ (monotone in the key)
+  const int nbits = 32 - __clz(lo ^ hi);
+  const int shift = nbits > 11 ? nbits - 11 : 0;
+  auto bin_of = [&](uint32_t key) -> unsigned { return (key - lo) >> shift; };
+  for (int i = tid; i < n; i += kTopkThreads) atomicAdd(&fs.bins[bin_of(keys[i])], 1u);
+  __syncthreads();
+  // thread t owns bins 4t .. 4t+3; counts above each bin, from the top bin down
+  unsigned c[4], own = 0;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    c[u] = fs.bins[4 * tid + u];
+    own += c[u];
+  }
+  unsigned incl = own;  // sum over this lane and the higher lanes of the warp
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned y = __shfl_down_sync(0xffffffffu, incl, o);
+    if (lane + o < 32) incl += y;
+  }
+  if (lane == 0) fs.wsum[warp] = (int)incl;
+  __syncthreads();
+  unsigned above = incl - own;
+  for (int w = warp + 1; w < kWarps; ++w) above += (unsigned)fs.wsum[w];
+#pragma unroll
+  for (int u = 3; u >= 0; --u) {
+    if (above < (unsigned)k && (unsigned)k <= above + c[u]) {
+      fs.b_bin = 4 * tid + u;
+      fs.b_above = (int)above;
+    }
+    above += c[u];
+  }
+  __syncthreads();
+  const unsigned bstar = (unsigned)fs.b_bin;
+  const int need = k - fs.b_above;
+  const unsigned m = fs.bins[bstar];
+  if (m > 256u) {
+    block_select(keys, n, k, sh, emit, select_trace_err);
+    return;
+  }
+  // the boundary bin's keys, ranked among themselves
+  for (int i = tid; i < n; i += kTopkThreads) {
+    const uint32_t key = keys[i];
+    if (bin_of(key) == bstar) {
+      const int pos = atomicAdd(&fs.b_cnt, 1);
+      fs.bkey[pos] = key;
+      fs.bidx[pos] = i;
+    }
+  }
+  __syncthreads();
+  if (tid < (int)m) {
+    const uint32_t mk = fs.bkey[tid];
+    const int mi = fs.bidx[tid];
+    int rank = 0;
+    for (int u = 0; u < (int)m; ++u) {
+      const uint32_t ok = fs.bkey[u];
+      rank += (ok > mk) || (ok == mk && fs.bidx[u] < mi);
+    }
+    bflag[mi] = rank < need ? 1 : 0;
+  }
+  __syncthreads();
+  // ordered compaction over contiguous ranges
+  const int ipt = (n + kTopkThreads - 1) / kTopkThreads;
+  const int i0 = min(n, tid * ipt), i1 = min(n, i0 + ipt);
+  auto taken = [&](int i) {
+    const unsigned bin = bin_of(keys[i]);
+    return bin > bstar || (bin == bstar && bflag[i]);
+  };
+  int cnt = 0;
+  for (int i = i0; i < i1; ++i) cnt += taken(i);
+  int total;
+  int pos = block_exclusive_scan(cnt, sh.warp_tmp, total);
+  for (int i = i0; i < i1; ++i)
+    if (taken(i)) emit(pos++, i);
+  if (tid == 0) {
+    trace_add(select_trace_err, kTrSelRadix, trace_clock() - tc0);
+    trace_add(select_trace_err, kTrSelCalls, 1ull);
+  }
+}
+
 // GT: heads per group (compile time; 0 = any G <= 16 at run time).
 // Each thread owns IPT consecutive pages of the chunk, whose s_hat rows it
 // loads together with the lengths and the scan partials in one round trip.
@@ -213,7 +342,9 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs a) {
   extern __shared__ __align__(16) uint8_t dyn[];
   uint32_t* keys = reinterpret_cast<uint32_t*>(dyn);
   int32_t* idx = reinterpret_cast<int32_t*>(dyn + a.smem_keys * sizeof(uint32_t));
+  uint8_t* bflag = dyn + a.smem_keys * (sizeof(uint32_t) + sizeof(int32_t));
   __shared__ SelectShared sh;
+  __shared__ FastShared fsh;
   __shared__ float zsh[16];
   __shared__ int is_last;
 
@@ -338,7 +469,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs a) {
 
   const int kloc = k < nloc ? k : nloc;
   if (a.n_chunks == 1) {
-    block_select(keys, nloc, kloc, sh, [&](int pos, int i) { sel[pos] = j0 + i; }, a.err);
+    fast_select(keys, bflag, nloc, kloc, sh, fsh, [&](int pos, int i) { sel[pos] = j0 + i; }, a.err);
     if (tid == 0) a.sel_count[bh] = kloc;
     trace_mark(a.err, kTrTopkSelected, false);
     trace_mark(a.err, kTrTopkExit, false);
@@ -347,7 +478,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs a) {
 
   uint32_t* ck = a.cand_key + ((size_t)bh * a.n_chunks + chunk) * a.k_max;
   int32_t* ci = a.cand_idx + ((size_t)bh * a.n_chunks + chunk) * a.k_max;
-  block_select(keys, nloc, kloc, sh, [&](int pos, int i) {
+  fast_select(keys, bflag, nloc, kloc, sh, fsh, [&](int pos, int i) {
     ck[pos] = keys[i];
     ci[pos] = j0 + i;
   });
@@ -386,7 +517,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs a) {
     }
   }
   __syncthreads();
-  block_select(keys, n_all, k, sh, [&](int pos, int i) { sel[pos] = idx[i]; });
+  fast_select(keys, bflag, n_all, k, sh, fsh, [&](int pos, int i) { sel[pos] = idx[i]; });
   if (tid == 0) {
     a.sel_count[bh] = k;
     a.counters[bh] = 0;  // ready for the next call
@@ -396,7 +527,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs a) {
 
 }  // namespace
 
-size_t topk_smem_bytes(size_t keys) { return keys * (sizeof(uint32_t) + sizeof(int32_t)); }
+// keys (u32), their positions (i32) and boundary-bin flags (u8)
+size_t topk_smem_bytes(size_t keys) { return keys * (sizeof(uint32_t) + sizeof(int32_t) + 1); }
 
 namespace {
 
