@@ -222,6 +222,39 @@ LOCKS_API locks_status_t locks_dense_decode(const locks_cache_t* cache, const lo
 LOCKS_API locks_status_t locks_exact_page_lse(const locks_cache_t* cache, const locks_params_t* params,
                                     const void* q, float* page_lse, void* stream);
 
+/* Capacity, in bytes, of the library's own static device workspace used by
+ * locks_decode_step_static. */
+#define LOCKS_STATIC_WS_BYTES ((size_t)8 << 20)
+
+/* locks_decode_step for callers that cannot allocate device memory: hosts
+ * that keep every byte of the GPU in their own pool and forbid outside
+ * allocations, or thin C callers with no way to keep a workspace alive
+ * between calls.  The paper has no counterpart; this is a convenience of
+ * this library.
+ *
+ * Same arguments and results as locks_decode_step, minus the workspace: the
+ * step runs in a fixed array of LOCKS_STATIC_WS_BYTES (8 MiB) that the
+ * library holds on every GPU it is loaded on, until the process exits.
+ * Nothing is allocated or freed: no cudaMalloc, cudaFree or allocating
+ * library routine is called.
+ *   - The first call on a device (with that device current) looks up the
+ *     array's device address; make it before any stream capture begins.
+ *   - Each call first zeroes the part of the array these shapes use (one
+ *     cudaMemsetAsync on `stream`), so it does not depend on what an earlier
+ *     call left there.
+ *   - Every call on a device shares the one array: calls that overlap on the
+ *     GPU (different streams, or different threads without ordering) race
+ *     and give wrong results.  Order them on one stream.
+ *   - Shapes whose workspace (locks_workspace_size) exceeds
+ *     LOCKS_STATIC_WS_BYTES return LOCKS_ERR_WORKSPACE before any GPU work;
+ *     use locks_decode_step with a caller-owned workspace for those.
+ *   - device_error: optional device int32; receives this call's
+ *     LOCKS_DEVERR_* bits (0 when none).  NULL to skip. */
+LOCKS_API locks_status_t locks_decode_step_static(const locks_cache_t* cache, const locks_summary_t* summary,
+                                                  const locks_params_t* params, const void* q, void* out,
+                                                  float* lse, int32_t* sel_pages, int32_t* sel_count,
+                                                  int32_t* device_error, void* stream);
+
 /* Read (and clear) the workspace's device error word.  Synchronises `stream`.
  * *code receives the LOCKS_DEVERR_* bits; returns LOCKS_ERR_DEVICE when any
  * bit was set, LOCKS_OK otherwise.  Not capturable. */

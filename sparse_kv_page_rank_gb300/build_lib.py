@@ -24,7 +24,7 @@ LIB = os.path.join(OUT_DIR, "liblocks.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
           "--expt-relaxed-constexpr"]
-SOURCES = ["api.cu", "scan.cu", "topk.cu", "attend.cu", "build.cu"]
+SOURCES = ["api.cu", "scan.cu", "topk.cu", "attend.cu", "build.cu", "static_ws.cu"]
 
 
 def nvcc() -> str:

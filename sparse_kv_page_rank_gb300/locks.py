@@ -24,6 +24,8 @@ LOCKS_ERR_UNSUPPORTED = 2
 LOCKS_ERR_CUDA = 3
 LOCKS_ERR_WORKSPACE = 4
 LOCKS_ERR_DEVICE = 5
+# bytes of the library-owned workspace behind locks_decode_step_static
+LOCKS_STATIC_WS_BYTES = 8 << 20
 LOCKS_DTYPE_BF16 = 0
 LOCKS_DTYPE_F32 = 1
 LOCKS_DEVERR_BLOCK_TABLE = 0x1
@@ -84,6 +86,7 @@ def lib() -> ctypes.CDLL:
             "locks_dense_decode": (ctypes.c_int, [C, R, vp, vp, vp, vp, sz, vp]),
             "locks_exact_page_lse": (ctypes.c_int, [C, R, vp, vp, vp]),
             "locks_get_device_error": (ctypes.c_int, [vp, P(i32), vp]),
+            "locks_decode_step_static": (ctypes.c_int, [C, S, R, vp, vp, vp, vp, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -183,6 +186,15 @@ def locks_decode_step(cache, summary, params, q, out, lse, sel_pages, sel_count,
     _check(lib().locks_decode_step(ctypes.byref(cache), ctypes.byref(summary), ctypes.byref(params), _ptr(q),
                                    _ptr(out), _ptr(lse), _ptr(sel_pages), _ptr(sel_count), _ptr(ws),
                                    int(ws_bytes), _stream(stream)), "locks_decode_step")
+
+
+def locks_decode_step_static(cache, summary, params, q, out, lse, sel_pages=None, sel_count=None,
+                             device_error=None, stream=None):
+    """locks_decode_step in the library's own fixed device workspace (no
+    workspace argument; for callers that cannot allocate device memory)."""
+    _check(lib().locks_decode_step_static(ctypes.byref(cache), ctypes.byref(summary), ctypes.byref(params),
+                                          _ptr(q), _ptr(out), _ptr(lse), _ptr(sel_pages), _ptr(sel_count),
+                                          _ptr(device_error), _stream(stream)), "locks_decode_step_static")
 
 
 def locks_dense_decode(cache, params, q, out, lse, ws, ws_bytes: int, stream=None):
