@@ -49,8 +49,8 @@ P, D = 64, 128
 # DRAM traffic of one summary-scan launch per summarised page-head (bytes),
 # from an ncu capture of the scan kernel (profiles/scan_kernel_llama128k.md);
 # valid only while scan.cu is unchanged since that capture.
-SCAN_TRAFFIC_PER_PAGE_HEAD = None
-SCAN_TRAFFIC_SOURCE_SHA = None
+SCAN_TRAFFIC_PER_PAGE_HEAD = 50365952 / 16384
+SCAN_TRAFFIC_SOURCE_SHA = "6bb8745f67c39b86"
 
 
 # ---------------------------------------------------------------------------
