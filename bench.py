@@ -383,6 +383,11 @@ def run_gpu(args):
         out_host.copy_(rt.out, non_blocking=True)
 
     e2e_ms_dev = timed(e2e_fn, K, W)
+    # every timed call must have finished without a device-side error
+    # (a bounded wait that ran out, or a bad block-table entry)
+    errs = [rt_.device_error() for rt_ in rts]
+    if any(errs):
+        raise SystemExit(f"device error bits {errs} after the timed steps: this run is invalid")
 
     # quality: mass recall of the selected pages against the exact page LSE
     # (read-every-key, on the GPU), and carrier retention

@@ -42,9 +42,15 @@ namespace locks {
 
 namespace {
 
+// The slot count is a multiple of the consumer-warp count: page p goes to slot
+// p mod kSlots and to warp p mod kScanWarps, so every slot is always consumed
+// by the same warp, which therefore waits on the slot's phases strictly in
+// order.  (With a slot shared by several warps, a warp could wait on the
+// parity of a slot's next phase while the current one is still incomplete;
+// a parity wait on a phase two ahead returns at once, on stale data.)
 template <bool R16>
 struct Ring {
-  static constexpr int kSlots = R16 ? 16 : 32;     // page-heads in flight per CTA
+  static constexpr int kSlots = R16 ? 2 * kScanWarps : 4 * kScanWarps;  // page-heads in flight per CTA
   static constexpr int kCoef = R16 ? 4096 : 2048;  // basis block (r rows x 256 B) comes first
   static constexpr int kSlot = R16 ? 6144 : 3072;
 };
@@ -228,6 +234,7 @@ template <bool G16, bool R16, bool GRP2>
 __global__ void __launch_bounds__(kScanThreads, 2) scan_kernel(const ScanArgs a) {
   using RG = Ring<R16>;
   constexpr int S = RG::kSlots;
+  static_assert(S <= 32 && S % kScanWarps == 0, "one producer lane per slot; one consumer warp per slot");
   extern __shared__ uint8_t ring_raw[];
   __shared__ float2 red[kScanWarps][16];
   __shared__ __align__(8) uint64_t full_bar[S], empty_bar[S];
