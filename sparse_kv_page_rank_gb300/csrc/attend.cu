@@ -39,6 +39,12 @@ constexpr int kTile = 2 * kHalfTile;       // one page-head of K (or V): 16 KiB
 constexpr int kStage = 2 * kTile;          // K + V
 constexpr int kOStride = 132;              // padded row of the per-warp O buffer (floats)
 constexpr int kOctaOff = kWarps * 16 * kOStride * 4;  // CTA-level O [16][128] after the warp buffers
+// Sparse mode: what the other CTAs of the cluster push to this one, after the
+// stage ring (never aliased): O columns [rank][head][cols], (m, l) [rank][head]
+// and the barrier their arrivals complete.
+constexpr int kRecvO = 16 * kHeadDim * 4;
+constexpr int kRecvMl = 16 * 16 * 8;
+constexpr int kRecvBytes = kRecvO + kRecvMl + 16;
 
 __device__ __forceinline__ uint32_t tile_addr(uint32_t base, int row, int chunk16) {
   // 128B swizzle: 16-byte chunk index XOR (row mod 8) within each 128-byte row
@@ -115,9 +121,14 @@ __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_con
     prefetch_tmap(&tk);
     if (MODE != kAttendPageLse) prefetch_tmap(&tv);
     for (int s = 0; s < STAGES; ++s) mbar_init(&bars[s], 1);
+    if (MODE == kAttendSparse)
+      mbar_init(reinterpret_cast<uint64_t*>(smem + STAGES * kStage + kRecvO + kRecvMl), a.cluster);
     fence_mbar_init();
   }
   __syncthreads();
+  // sparse mode: every CTA's receive barrier must be initialised before any
+  // other CTA of the cluster arrives on it (the matching wait comes at the merge)
+  if (MODE == kAttendSparse) cluster_arrive();
 
   // Inside the fused step the step's own inputs (q, lengths, block table) were
   // written before its first kernel started, so they can be read while the
@@ -409,6 +420,54 @@ __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_con
   // ---- merge the CTAs of the cluster through distributed shared memory ----
   const int CS = a.cluster, NC = a.n_splits / a.cluster;
   const uint32_t rank = cluster_ctarank();
+  if (MODE == kAttendSparse) {
+    // One cluster per problem.  Each CTA pushes its partial state to the
+    // CTAs that own its output columns (rank r owns columns [r*cols,
+    // (r+1)*cols)) and arrives on their receive barriers; each CTA then
+    // waits for all CS contributions and merges its columns from its own
+    // shared memory.  Nobody reads another CTA's memory, so no CTA has to
+    // wait for the others before it exits.
+    const int cols = kHeadDim / CS;
+    float* recv_o = reinterpret_cast<float*>(smem + STAGES * kStage);
+    float2* recv_ml = reinterpret_cast<float2*>(smem + STAGES * kStage + kRecvO);
+    uint64_t* recv_bar = reinterpret_cast<uint64_t*>(smem + STAGES * kStage + kRecvO + kRecvMl);
+    cluster_wait();  // every CTA's receive barrier is initialised
+    const uint32_t ro = smem_u32(recv_o), rml = smem_u32(recv_ml);
+    for (int e = tid; e < G * (kHeadDim / 4); e += kAttendThreads) {
+      const int h = e / (kHeadDim / 4), c4 = 4 * (e % (kHeadDim / 4));
+      const int dst = c4 / cols, cc = c4 % cols;
+      const float4 v = *reinterpret_cast<const float4*>(octa + h * kHeadDim + c4);
+      st_dsmem_f4(dsmem_addr(ro + 4 * (((int)rank * G + h) * cols + cc), dst), v);
+    }
+    for (int e = tid; e < CS * G; e += kAttendThreads) {
+      const int dst = e / G, h = e % G;
+      st_dsmem_f2(dsmem_addr(rml + 8 * ((int)rank * 16 + h), dst), make_float2(cta_m[h], cta_l[h]));
+    }
+    __syncthreads();  // the whole CTA's stores precede the release arrivals
+    if (tid < CS) mbar_arrive_remote(dsmem_addr(smem_u32(recv_bar), tid));
+    if (!mbar_wait_cluster(recv_bar, 0) && tid == 0) set_error(a.err, kDevErrTimeout);
+    if (MODE == kAttendSparse) trace_mark(a.err, kTrAttClusterMerged, false);
+    for (int e = tid; e < G * cols; e += kAttendThreads) {
+      const int h = e / cols, cc = e % cols, col = (int)rank * cols + cc;
+      float M = -INFINITY;
+      for (int rr = 0; rr < CS; ++rr) M = fmaxf(M, recv_ml[rr * 16 + h].x);
+      float Ls = 0.f, O = 0.f;
+      if (M != -INFINITY) {
+        for (int rr = 0; rr < CS; ++rr) {
+          const float2 ml = recv_ml[rr * 16 + h];
+          const float f = fast_exp2(ml.x - M);
+          Ls += ml.y * f;
+          O += recv_o[(rr * G + h) * cols + cc] * f;
+        }
+      }
+      const size_t oi = ((size_t)b * Hq + (size_t)hkv * G + h);
+      const float val = Ls > 0.f ? O / Ls : 0.f;
+      a.out[oi * kHeadDim + col] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
+      if (a.lse && col == 0) a.lse[oi] = (Ls > 0.f) ? (M + fast_log2(Ls)) * kLn2 : -INFINITY;
+    }
+    if (MODE == kAttendSparse) trace_mark(a.err, kTrAttExit, false);
+    return;
+  }
   const int q = split / CS;
   const int cols = kHeadDim / CS, c0 = (int)rank * cols;
   cluster_sync();
@@ -492,7 +551,7 @@ __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_con
 
 template <int MODE, int STAGES>
 size_t smem_bytes() {
-  return (size_t)STAGES * kStage + 1024;
+  return (size_t)STAGES * kStage + 1024 + (MODE == kAttendSparse ? kRecvBytes : 0);
 }
 
 template <int MODE, int STAGES>

@@ -203,25 +203,34 @@ __device__ void block_select(const uint32_t* keys, int n, int k, SelectShared& s
   }
 }
 
-// Faster selection for the common case.  One histogram pass over the top 11
-// bits in which the keys differ (2048 bins) finds the bin that holds the k-th
-// largest key; keys in higher bins are all taken, and the few keys of that
-// boundary bin are ranked against each other (key descending, position
-// ascending) to take the rest.  When the boundary bin holds more than 256
-// keys (many equal or nearly equal keys) the radix select above is used.
-// Output order and ties are as in block_select.
-struct FastShared {
+// Faster selection for the common case, with the keys in registers: key u
+// of thread t is element t + kTopkThreads * u.  One histogram of the top 11
+// bits in which the keys differ (2048 bins) finds the bin that holds the
+// k-th largest key; keys in higher bins are all taken, and the few keys of
+// that boundary bin are ranked against each other (key descending, element
+// ascending) to take the rest.  The chosen elements are then numbered in
+// element order with warp ballots.  When the boundary bin holds more than
+// kBoundaryMax keys (many equal or nearly equal keys) the radix select above
+// runs instead, on the same keys in shared memory (`keys_smem`).  Output
+// order and ties are as in block_select.
+constexpr int kBoundaryMax = 256;
+struct __align__(16) FastShared {
   unsigned bins[2048];
-  uint32_t bkey[256];
-  int bidx[256];
+  uint32_t bkey[kBoundaryMax];
+  int bidx[kBoundaryMax];
+  unsigned char bwin[kBoundaryMax];
   int wsum[kWarps];
   unsigned wmin[kWarps], wmax[kWarps];
+  int cnt[128];  // chosen elements per (u, warp) block, u-major
   int b_bin, b_above, b_cnt;
 };
 
-template <typename Emit>
-__device__ void fast_select(const uint32_t* keys, uint8_t* bflag, int n, int k, SelectShared& sh,
-                            FastShared& fs, Emit emit, int* select_trace_err = nullptr) {
+template <int IPT, typename Emit>
+__device__ void reg_select(const uint32_t (&kr)[IPT], const uint32_t* keys_smem, int n, int k, SelectShared& sh,
+                           FastShared& fs, Emit emit, int* select_trace_err = nullptr) {
+  constexpr int E = IPT * kWarps;         // blocks of 32 consecutive elements
+  constexpr int EPL = (E + 31) / 32;      // blocks per lane in the prefix sum
+  static_assert(E <= 128, "per-block counts must fit");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (k <= 0 || n <= 0) return;
   if (k >= n) {
@@ -230,10 +239,12 @@ __device__ void fast_select(const uint32_t* keys, uint8_t* bflag, int n, int k, 
   }
   const unsigned long long tc0 = trace_clock();
   unsigned lo = 0xffffffffu, hi = 0u;
-  for (int i = tid; i < n; i += kTopkThreads) {
-    const uint32_t key = keys[i];
-    lo = min(lo, key);
-    hi = max(hi, key);
+#pragma unroll
+  for (int u = 0; u < IPT; ++u) {
+    if (tid + kTopkThreads * u < n) {
+      lo = min(lo, kr[u]);
+      hi = max(hi, kr[u]);
+    }
   }
   lo = __reduce_min_sync(0xffffffffu, lo);
   hi = __reduce_max_sync(0xffffffffu, hi);
@@ -241,7 +252,7 @@ __device__ void fast_select(const uint32_t* keys, uint8_t* bflag, int n, int k, 
     fs.wmin[warp] = lo;
     fs.wmax[warp] = hi;
   }
-  for (int b = tid; b < 2048; b += kTopkThreads) fs.bins[b] = 0;
+  reinterpret_cast<uint4*>(fs.bins)[tid] = make_uint4(0u, 0u, 0u, 0u);
   if (tid == 0) fs.b_cnt = 0;
   __syncthreads();
 #pragma unroll
@@ -249,23 +260,24 @@ __device__ void fast_select(const uint32_t* keys, uint8_t* bflag, int n, int k, 
     lo = min(lo, fs.wmin[w]);
     hi = max(hi, fs.wmax[w]);
   }
-  if (lo == hi) {  // all keys equal: the first k positions
+  if (lo == hi) {  // all keys equal: the first k elements
     for (int i = tid; i < k; i += kTopkThreads) emit(i, i);
     return;
   }
   // bins: the top 11 of the bits in which the keys differ (monotone in the key)
   const int nbits = 32 - __clz(lo ^ hi);
   const int shift = nbits > 11 ? nbits - 11 : 0;
-  auto bin_of = [&](uint32_t key) -> unsigned { return (key - lo) >> shift; };
-  for (int i = tid; i < n; i += kTopkThreads) atomicAdd(&fs.bins[bin_of(keys[i])], 1u);
+  unsigned bin[IPT];
+#pragma unroll
+  for (int u = 0; u < IPT; ++u) {
+    bin[u] = (kr[u] - lo) >> shift;
+    if (tid + kTopkThreads * u < n) atomicAdd(&fs.bins[bin[u]], 1u);
+  }
   __syncthreads();
   // thread t owns bins 4t .. 4t+3; counts above each bin, from the top bin down
-  unsigned c[4], own = 0;
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    c[u] = fs.bins[4 * tid + u];
-    own += c[u];
-  }
+  const uint4 c4 = reinterpret_cast<const uint4*>(fs.bins)[tid];
+  const unsigned c[4] = {c4.x, c4.y, c4.z, c4.w};
+  const unsigned own = c[0] + c[1] + c[2] + c[3];
   unsigned incl = own;  // sum over this lane and the higher lanes of the warp
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -275,7 +287,9 @@ __device__ void fast_select(const uint32_t* keys, uint8_t* bflag, int n, int k, 
   if (lane == 0) fs.wsum[warp] = (int)incl;
   __syncthreads();
   unsigned above = incl - own;
-  for (int w = warp + 1; w < kWarps; ++w) above += (unsigned)fs.wsum[w];
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w)
+    if (w > warp) above += (unsigned)fs.wsum[w];
 #pragma unroll
   for (int u = 3; u >= 0; --u) {
     if (above < (unsigned)k && (unsigned)k <= above + c[u]) {
@@ -288,17 +302,27 @@ __device__ void fast_select(const uint32_t* keys, uint8_t* bflag, int n, int k, 
   const unsigned bstar = (unsigned)fs.b_bin;
   const int need = k - fs.b_above;
   const unsigned m = fs.bins[bstar];
-  if (m > 256u) {
-    block_select(keys, n, k, sh, emit, select_trace_err);
+  if (m > (unsigned)kBoundaryMax) {
+    block_select(keys_smem, n, k, sh, emit, select_trace_err);
     return;
   }
-  // the boundary bin's keys, ranked among themselves
-  for (int i = tid; i < n; i += kTopkThreads) {
-    const uint32_t key = keys[i];
-    if (bin_of(key) == bstar) {
-      const int pos = atomicAdd(&fs.b_cnt, 1);
-      fs.bkey[pos] = key;
-      fs.bidx[pos] = i;
+  // the boundary bin's keys into a short list (one atomic per warp and u)
+  int bslot[IPT];
+#pragma unroll
+  for (int u = 0; u < IPT; ++u) {
+    bslot[u] = -1;
+    if (kTopkThreads * u >= n) continue;  // uniform over the block
+    const bool eq = tid + kTopkThreads * u < n && bin[u] == bstar;
+    const unsigned mask = __ballot_sync(0xffffffffu, eq);
+    int base = 0;
+    if (mask) {
+      if (lane == 0) base = atomicAdd(&fs.b_cnt, __popc(mask));
+      base = __shfl_sync(0xffffffffu, base, 0);
+    }
+    bslot[u] = eq ? base + __popc(mask & ((1u << lane) - 1u)) : -1;
+    if (eq) {
+      fs.bkey[bslot[u]] = kr[u];
+      fs.bidx[bslot[u]] = tid + kTopkThreads * u;
     }
   }
   __syncthreads();
@@ -306,26 +330,59 @@ __device__ void fast_select(const uint32_t* keys, uint8_t* bflag, int n, int k, 
     const uint32_t mk = fs.bkey[tid];
     const int mi = fs.bidx[tid];
     int rank = 0;
-    for (int u = 0; u < (int)m; ++u) {
-      const uint32_t ok = fs.bkey[u];
-      rank += (ok > mk) || (ok == mk && fs.bidx[u] < mi);
+    for (int v = 0; v < (int)m; ++v) {
+      const uint32_t ok = fs.bkey[v];
+      rank += (ok > mk) || (ok == mk && fs.bidx[v] < mi);
     }
-    bflag[mi] = rank < need ? 1 : 0;
+    fs.bwin[tid] = rank < need ? 1 : 0;
   }
   __syncthreads();
-  // ordered compaction over contiguous ranges
-  const int ipt = (n + kTopkThreads - 1) / kTopkThreads;
-  const int i0 = min(n, tid * ipt), i1 = min(n, i0 + ipt);
-  auto taken = [&](int i) {
-    const unsigned bin = bin_of(keys[i]);
-    return bin > bstar || (bin == bstar && bflag[i]);
-  };
-  int cnt = 0;
-  for (int i = i0; i < i1; ++i) cnt += taken(i);
-  int total;
-  int pos = block_exclusive_scan(cnt, sh.warp_tmp, total);
-  for (int i = i0; i < i1; ++i)
-    if (taken(i)) emit(pos++, i);
+  // number the chosen elements in element order: element t + 512u sits in
+  // block (u, warp) of 32 consecutive elements, blocks ordered u-major
+  bool take[IPT];
+#pragma unroll
+  for (int u = 0; u < IPT; ++u) {
+    take[u] = false;
+    if (kTopkThreads * u >= n) {
+      if (lane == 0) fs.cnt[u * kWarps + warp] = 0;
+      continue;
+    }
+    take[u] = tid + kTopkThreads * u < n && (bin[u] > bstar || (bslot[u] >= 0 && fs.bwin[bslot[u]]));
+    const unsigned mask = __ballot_sync(0xffffffffu, take[u]);
+    if (lane == 0) fs.cnt[u * kWarps + warp] = __popc(mask);
+  }
+  __syncthreads();
+  // exclusive prefix over the E block counts, lane l holding blocks
+  // EPL*l .. EPL*l + EPL - 1 (every warp computes it)
+  int ex[EPL];
+  int own2 = 0;
+#pragma unroll
+  for (int v = 0; v < EPL; ++v) {
+    const int e = EPL * lane + v;
+    ex[v] = own2;
+    own2 += e < E ? fs.cnt[e] : 0;
+  }
+  int incl2 = own2;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl2, o);
+    if (lane >= o) incl2 += y;
+  }
+#pragma unroll
+  for (int v = 0; v < EPL; ++v) ex[v] += incl2 - own2;
+#pragma unroll
+  for (int u = 0; u < IPT; ++u) {
+    if (kTopkThreads * u >= n) break;  // uniform over the block
+    const int e = u * kWarps + warp;
+    int base = 0;
+#pragma unroll
+    for (int v = 0; v < EPL; ++v) {
+      const int t = __shfl_sync(0xffffffffu, ex[v], e / EPL);
+      if (e % EPL == v) base = t;
+    }
+    const unsigned mask = __ballot_sync(0xffffffffu, take[u]);
+    if (take[u]) emit(base + __popc(mask & ((1u << lane) - 1u)), tid + kTopkThreads * u);
+  }
   if (tid == 0) {
     trace_add(select_trace_err, kTrSelRadix, trace_clock() - tc0);
     trace_add(select_trace_err, kTrSelCalls, 1ull);
@@ -342,7 +399,6 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs a) {
   extern __shared__ __align__(16) uint8_t dyn[];
   uint32_t* keys = reinterpret_cast<uint32_t*>(dyn);
   int32_t* idx = reinterpret_cast<int32_t*>(dyn + a.smem_keys * sizeof(uint32_t));
-  uint8_t* bflag = dyn + a.smem_keys * (sizeof(uint32_t) + sizeof(int32_t));
   __shared__ SelectShared sh;
   __shared__ FastShared fsh;
   __shared__ float zsh[16];
@@ -441,6 +497,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs a) {
   // sigma_j = ln( (1/G) sum_h exp(s_hat[h][j] - Z_h) ) -> order-preserving keys
   const int j1 = min(j0 + a.chunk_pages, ns);
   const int nloc = j1 > j0 ? j1 - j0 : 0;
+  uint32_t kr[IPT];  // this thread's keys: page j0 + tid + kTopkThreads * p
   {
     const float log2G = log2f((float)G);
     float zl[GMAX];
@@ -460,7 +517,10 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs a) {
         float acc = 0.f;
 #pragma unroll
         for (int h = 0; h < GMAX; ++h) acc += h < G ? fast_exp2(y[h] - mx) : 0.f;
-        keys[jl] = orderable_key((mx + fast_log2(acc) - log2G) * kLn2);
+        kr[p] = orderable_key((mx + fast_log2(acc) - log2G) * kLn2);
+        keys[jl] = kr[p];
+      } else {
+        kr[p] = 0u;
       }
     }
   }
@@ -469,7 +529,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs a) {
 
   const int kloc = k < nloc ? k : nloc;
   if (a.n_chunks == 1) {
-    fast_select(keys, bflag, nloc, kloc, sh, fsh, [&](int pos, int i) { sel[pos] = j0 + i; }, a.err);
+    reg_select<IPT>(kr, keys, nloc, kloc, sh, fsh, [&](int pos, int i) { sel[pos] = j0 + i; }, a.err);
     if (tid == 0) a.sel_count[bh] = kloc;
     trace_mark(a.err, kTrTopkSelected, false);
     trace_mark(a.err, kTrTopkExit, false);
@@ -478,7 +538,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs a) {
 
   uint32_t* ck = a.cand_key + ((size_t)bh * a.n_chunks + chunk) * a.k_max;
   int32_t* ci = a.cand_idx + ((size_t)bh * a.n_chunks + chunk) * a.k_max;
-  fast_select(keys, bflag, nloc, kloc, sh, fsh, [&](int pos, int i) {
+  reg_select<IPT>(kr, keys, nloc, kloc, sh, fsh, [&](int pos, int i) {
     ck[pos] = keys[i];
     ci[pos] = j0 + i;
   });
@@ -517,7 +577,14 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs a) {
     }
   }
   __syncthreads();
-  fast_select(keys, bflag, n_all, k, sh, fsh, [&](int pos, int i) { sel[pos] = idx[i]; });
+  auto emit_merged = [&](int pos, int i) { sel[pos] = idx[i]; };
+  if (n_all <= IPT * kTopkThreads) {
+#pragma unroll
+    for (int u = 0; u < IPT; ++u) kr[u] = tid + kTopkThreads * u < n_all ? keys[tid + kTopkThreads * u] : 0u;
+    reg_select<IPT>(kr, keys, n_all, k, sh, fsh, emit_merged);
+  } else {
+    block_select(keys, n_all, k, sh, emit_merged);
+  }
   if (tid == 0) {
     a.sel_count[bh] = k;
     a.counters[bh] = 0;  // ready for the next call
@@ -527,8 +594,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs a) {
 
 }  // namespace
 
-// keys (u32), their positions (i32) and boundary-bin flags (u8)
-size_t topk_smem_bytes(size_t keys) { return keys * (sizeof(uint32_t) + sizeof(int32_t) + 1); }
+// keys (u32) and their positions (i32)
+size_t topk_smem_bytes(size_t keys) { return keys * (sizeof(uint32_t) + sizeof(int32_t)); }
 
 namespace {
 
