@@ -118,9 +118,11 @@ Plan make_plan(const locks_cache_t* c, const locks_params_t* p) {
     const int cs_sparse = attend_max_cluster(kAttendSparse);
     const int cs_dense = attend_max_cluster(kAttendDense);
     const long long items = (long long)pl.k_max + 2;
+    // the largest cluster (up to one CTA per item) with which every
+    // problem's cluster is resident at once: one wave, no CTA waits for a slot
     int cs = 1;
     while (cs * 2 <= cs_sparse && cs * 2 <= items) cs *= 2;
-    while (cs > 1 && BH * cs > 2 * target) cs /= 2;
+    while (cs > 1 && BH > attend_active_clusters(kAttendSparse, cs)) cs /= 2;
     pl.sparse_cluster = cs;
     // dense: the (cluster, clusters-per-problem) shape with the most CTAs
     // that still fits in one wave of `target` resident CTAs

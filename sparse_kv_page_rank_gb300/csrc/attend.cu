@@ -394,25 +394,36 @@ __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_con
     *reinterpret_cast<float2*>(so + (warp * 16 + g + 8) * kOStride + col) = make_float2(o[nt][2], o[nt][3]);
   }
   __syncthreads();
-  for (int e = tid; e < G * kHeadDim; e += kAttendThreads) {
-    const int h = e / kHeadDim, d = e % kHeadDim;
+  // per head: the max over the warps and each warp's rescale factor, once
+  __shared__ float sm_f[kWarps][16];
+  if (tid < G) {
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w][h]);
-    float Ls = 0.f, O = 0.f;
-    if (M != -INFINITY) {
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w][tid]);
+    float Ls = 0.f;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float f = fast_exp2(sm_m[w][h] - M);
-        Ls += sm_l[w][h] * f;
-        O += so[(w * 16 + h) * kOStride + d] * f;
-      }
+    for (int w = 0; w < kWarps; ++w) {
+      const float f = (M == -INFINITY) ? 0.f : fast_exp2(sm_m[w][tid] - M);
+      sm_f[w][tid] = f;
+      Ls += sm_l[w][tid] * f;
     }
-    octa[h * kHeadDim + d] = O;
-    if (d == 0) {
-      cta_m[h] = M;
-      cta_l[h] = Ls;
+    cta_m[tid] = M;
+    cta_l[tid] = Ls;
+  }
+  __syncthreads();
+  for (int e = tid; e < G * (kHeadDim / 4); e += kAttendThreads) {
+    const int h = e / (kHeadDim / 4), d4 = 4 * (e % (kHeadDim / 4));
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float f = sm_f[w][h];
+      const float4 v = *reinterpret_cast<const float4*>(so + (w * 16 + h) * kOStride + d4);
+      O.x = fmaf(v.x, f, O.x);
+      O.y = fmaf(v.y, f, O.y);
+      O.z = fmaf(v.z, f, O.z);
+      O.w = fmaf(v.w, f, O.w);
     }
+    *reinterpret_cast<float4*>(octa + h * kHeadDim + d4) = O;
   }
   __syncthreads();
 
@@ -587,6 +598,34 @@ cudaError_t launch_mode(const AttendArgs& a, const CUtensorMap& tk, const CUtens
   return cudaLaunchKernelEx(&cfg, kern, tk, tv, a);
 }
 
+// How many clusters of cs CTAs of this kernel the device can hold at once
+// (0 when it cannot place one).
+template <int MODE, int STAGES>
+int active_clusters_of(int cs) {
+  auto kern = attend_kernel<MODE, STAGES>;
+  const size_t smem = smem_bytes<MODE, STAGES>();
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
+  if (cs > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cs, 1, 1);
+  cfg.blockDim = dim3(kAttendThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
 // Largest cluster size (16, 8, ... 1) the device can place for this kernel.
 template <int MODE, int STAGES>
 int max_cluster_of() {
@@ -618,6 +657,20 @@ constexpr int kSparseStages = 3;
 constexpr int kDenseStages = 2;
 
 }  // namespace
+
+int attend_active_clusters(int mode, int cs) {
+  static int cache[2][5][64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || cs < 1 || cs > 16) return 1;
+  const int m = mode == kAttendSparse ? 0 : 1;
+  const int li = 31 - __builtin_clz((unsigned)cs);
+  if (cache[m][li][dev] == 0) {
+    int n = mode == kAttendSparse ? active_clusters_of<kAttendSparse, kSparseStages>(cs)
+                                  : active_clusters_of<kAttendDense, kDenseStages>(cs);
+    cache[m][li][dev] = n > 0 ? n : -1;
+  }
+  return cache[m][li][dev] > 0 ? cache[m][li][dev] : 0;
+}
 
 int attend_max_cluster(int mode) {
   static int cache[2][64] = {};

@@ -87,6 +87,7 @@ cudaError_t launch_build(const BuildArgs& a, cudaStream_t s);
 size_t topk_smem_bytes(size_t keys);
 int topk_pages_per_cta(int group);  // pages one top-k CTA scores
 int attend_max_cluster(int mode);  // largest placeable cluster (<= 16) for that mode
+int attend_active_clusters(int mode, int cs);  // clusters of cs CTAs resident at once
 // Scan CTA: 7 consumer warps + 1 producer warp, so that two CTAs put four
 // warps on each SM sub-partition (whose register file is a quarter of the SM's).
 constexpr int kScanWarps = 7;
