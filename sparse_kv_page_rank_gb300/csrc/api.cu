@@ -38,7 +38,7 @@ struct Plan {
   size_t tk_keys = 0;
   int sparse_cluster = 1, dense_cluster = 1, dense_nc = 1, lse_splits = 1;
   size_t off_err = 0, off_cnt_tk = 0, off_cnt_att = 0, off_shat = 0, off_part = 0, off_ckey = 0,
-         off_cidx = 0, off_ccnt = 0, off_sel = 0, off_selcnt = 0, off_pml = 0, off_po = 0, total = 0;
+         off_cidx = 0, off_sel = 0, off_selcnt = 0, off_pml = 0, off_po = 0, total = 0;
 };
 
 locks_status_t check_cache(const locks_cache_t* c, bool need_kv) {
@@ -160,7 +160,6 @@ Plan make_plan(const locks_cache_t* c, const locks_params_t* p) {
   pl.off_part = take(sizeof(float2) * BH * pl.n_scan * pl.G);
   pl.off_ckey = take(sizeof(uint32_t) * BH * pl.n_tk * std::max(pl.k_max, 1));
   pl.off_cidx = take(sizeof(int32_t) * BH * pl.n_tk * std::max(pl.k_max, 1));
-  pl.off_ccnt = take(sizeof(int32_t) * BH * pl.n_tk);
   pl.off_sel = take(sizeof(int32_t) * BH * std::max(pl.k_max, 1));
   pl.off_selcnt = take(sizeof(int32_t) * BH);
   pl.off_pml = take(sizeof(float2) * BH * pl.dense_nc * pl.G);
@@ -250,7 +249,6 @@ locks_status_t run_select(const locks_cache_t* c, const locks_summary_t* s, cons
   ta.n_summarized = c->n_summarized;
   ta.cand_key = at<uint32_t>(ws, pl.off_ckey);
   ta.cand_idx = at<int32_t>(ws, pl.off_cidx);
-  ta.cand_cnt = at<int32_t>(ws, pl.off_ccnt);
   ta.counters = at<unsigned>(ws, pl.off_cnt_tk);
   ta.sel_pages = sel;
   ta.sel_count = selcnt;

@@ -33,7 +33,6 @@ struct TopkArgs {
   const int32_t* n_summarized;
   uint32_t* cand_key;   // ws: [B*Hkv][n_chunks][k_max]
   int32_t* cand_idx;    // ws: same
-  int32_t* cand_cnt;    // ws: [B*Hkv][n_chunks]
   unsigned* counters;   // ws: [B*Hkv]
   int32_t* sel_pages;   // [B*Hkv][k_max]
   int32_t* sel_count;   // [B*Hkv]

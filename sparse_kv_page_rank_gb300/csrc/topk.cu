@@ -393,7 +393,7 @@ __device__ void reg_select(const uint32_t (&kr)[IPT], const uint32_t* keys_smem,
 // Each thread owns IPT consecutive pages of the chunk, whose s_hat rows it
 // loads together with the lengths and the scan partials in one round trip.
 template <int GT>
-__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs a) {
+__global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkArgs a) {
   constexpr int GMAX = GT ? GT : 16;
   constexpr int IPT = GT ? (32 / GT < 8 ? 32 / GT : 8) : 2;  // pages per thread
   extern __shared__ __align__(16) uint8_t dyn[];
@@ -542,7 +542,12 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs a) {
     ck[pos] = keys[i];
     ci[pos] = j0 + i;
   });
-  if (tid == 0) a.cand_cnt[(size_t)bh * a.n_chunks + chunk] = kloc;
+  // unused candidate slots get the lowest key (never chosen: the chunks
+  // together always offer at least k real candidates)
+  for (int j = kloc + tid; j < a.k_max; j += kTopkThreads) {
+    ck[j] = 0u;
+    ci[j] = -1;
+  }
   __threadfence();
   __syncthreads();
   if (tid == 0) {
@@ -553,36 +558,29 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkArgs a) {
   if (!is_last) return;
   __threadfence();
 
-  // gather every chunk's candidates, in chunk (= page) order
-  __shared__ int s_cnt[64];
-  __shared__ int s_off[65];
-  for (int ch = tid; ch < a.n_chunks; ch += kTopkThreads)
-    if (ch < 64) s_cnt[ch] = __ldcg(a.cand_cnt + (size_t)bh * a.n_chunks + ch);
-  __syncthreads();
-  if (tid == 0) {
-    int o = 0;
-    for (int ch = 0; ch < a.n_chunks && ch < 64; ++ch) {
-      s_off[ch] = o;
-      o += s_cnt[ch];
-    }
-    s_off[a.n_chunks < 64 ? a.n_chunks : 64] = o;
-  }
-  __syncthreads();
-  const int n_all = s_off[a.n_chunks < 64 ? a.n_chunks : 64];
-  for (int e = tid; e < a.n_chunks * a.k_max; e += kTopkThreads) {
-    const int ch = e / a.k_max, i = e % a.k_max;
-    if (ch < 64 && i < s_cnt[ch]) {
-      keys[s_off[ch] + i] = __ldcg(a.cand_key + ((size_t)bh * a.n_chunks + ch) * a.k_max + i);
-      idx[s_off[ch] + i] = __ldcg(a.cand_idx + ((size_t)bh * a.n_chunks + ch) * a.k_max + i);
-    }
-  }
-  __syncthreads();
+  // every chunk's candidate slots, chunk-major (= page order), in one round trip
+  const int n_all = a.n_chunks * a.k_max;
+  const uint32_t* gk = a.cand_key + (size_t)bh * n_all;
+  const int32_t* gi = a.cand_idx + (size_t)bh * n_all;
   auto emit_merged = [&](int pos, int i) { sel[pos] = idx[i]; };
   if (n_all <= IPT * kTopkThreads) {
 #pragma unroll
-    for (int u = 0; u < IPT; ++u) kr[u] = tid + kTopkThreads * u < n_all ? keys[tid + kTopkThreads * u] : 0u;
+    for (int u = 0; u < IPT; ++u) {
+      const int i = tid + kTopkThreads * u;
+      kr[u] = 0u;
+      if (i < n_all) {
+        kr[u] = __ldcg(gk + i);
+        keys[i] = kr[u];
+        idx[i] = __ldcg(gi + i);
+      }
+    }
     reg_select<IPT>(kr, keys, n_all, k, sh, fsh, emit_merged);
   } else {
+    for (int i = tid; i < n_all; i += kTopkThreads) {
+      keys[i] = __ldcg(gk + i);
+      idx[i] = __ldcg(gi + i);
+    }
+    __syncthreads();
     block_select(keys, n_all, k, sh, emit_merged);
   }
   if (tid == 0) {
