@@ -46,11 +46,15 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
 P, D = 64, 128
 
-# DRAM traffic of one summary-scan launch per summarised page-head (bytes),
-# from an ncu capture of the scan kernel (profiles/scan_kernel_llama128k.md);
-# valid only while scan.cu is unchanged since that capture.
-SCAN_TRAFFIC_PER_PAGE_HEAD = 50365952 / 16384
-SCAN_TRAFFIC_SOURCE_SHA = "6bb8745f67c39b86"
+# DRAM traffic (bytes read + written) of one summary-scan launch per
+# summarised page-head, from ncu captures of the scan kernel on these
+# workloads (profiles/scan_kernel_llama128k.md, profiles/scan_kernel_ctx1m.md);
+# valid only while scan.cu is unchanged since those captures.
+SCAN_TRAFFIC_PER_PAGE_HEAD = {
+    "llama128k": (50372352 + 1536) / 16384,
+    "ctx1m": (100762112 + 3124480) / 32768,
+}
+SCAN_TRAFFIC_SOURCE_SHA = "085ec03a1bf11439"
 
 
 # ---------------------------------------------------------------------------
@@ -435,8 +439,8 @@ def run_gpu(args):
     scan_gbs = scan_alg / (scan_ms * 1e-3) / 1e9
     dense_gbs = db / (dense_ms * 1e-3) / 1e9
     traffic = None
-    if SCAN_TRAFFIC_PER_PAGE_HEAD is not None and SCAN_TRAFFIC_SOURCE_SHA == _scan_source_sha():
-        traffic = SCAN_TRAFFIC_PER_PAGE_HEAD * Hkv * n_sum_tot
+    if args.config in SCAN_TRAFFIC_PER_PAGE_HEAD and SCAN_TRAFFIC_SOURCE_SHA == _scan_source_sha():
+        traffic = SCAN_TRAFFIC_PER_PAGE_HEAD[args.config] * Hkv * n_sum_tot
 
     # CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only)
     cpu = None
