@@ -44,7 +44,8 @@ __all__ = [
     "exact_page_lse", "gsa_scores", "select_top_pages", "attention",
     "sparse_decode", "dense_decode", "decode_step", "build_summaries",
     "mass_recall", "carrier_retention", "shared_sketch_page_lse", "jacobi_eigh",
-    "reconstruction_error", "bf16_widen",
+    "reconstruction_error", "bf16_widen", "INT4_MAX", "INT8_MAX", "quantize_symmetric",
+    "quantize_summary", "dequantize_summary", "quantized_page_summary",
 ]
 
 RANK_DEFICIT_RTOL = 1e-6
@@ -128,6 +129,64 @@ def build_summaries(k_pool: np.ndarray, page_ids, r: int, centered: bool = False
         coeffs[p] = np.stack(cs)
         cent[p] = np.stack(ms)
     return basis, coeffs, cent
+
+
+# ---------------------------------------------------------------------------
+# Quantised summary ([expl] §2 "Implementatie", Kwantisatie: the basis is
+# stored in int4, the coefficients and the centroid in int8).  The pages give
+# no scale layout; the reading taken here: symmetric scales, one per basis
+# vector, one per coefficient column and one for the centroid, stored as
+# float32; s = max|x| / qmax with qmax = 7 (int4) or 127 (int8), and
+# q = round-half-to-even(x / s) clamped to [-qmax, qmax].  A zero vector has
+# s = 0 and q = 0.  The value a quantised summary stands for is q * s.
+# ---------------------------------------------------------------------------
+
+INT4_MAX = 7
+INT8_MAX = 127
+
+
+def quantize_symmetric(x: np.ndarray, qmax: int):
+    """One scale for the whole vector x: returns (q int64 array, s float)."""
+    x = np.asarray(x, dtype=np.float64)
+    amax = float(np.max(np.abs(x))) if x.size else 0.0
+    s = float(np.float32(amax / qmax)) if amax > 0 else 0.0
+    if s == 0.0:
+        return np.zeros(x.shape, dtype=np.int64), 0.0
+    q = np.clip(np.rint(x / s), -qmax, qmax).astype(np.int64)
+    return q, s
+
+
+def quantize_summary(V: np.ndarray, C: np.ndarray, mu: np.ndarray) -> dict:
+    """Quantise one page-head summary (V d x r, C P x r, centroid mu d).
+
+    Returns vq [r][d] (int4 values), sv [r], cq [P][r] (int8 values), sc [r],
+    muq [d] (int8 values), smu."""
+    d, r = V.shape
+    P = C.shape[0]
+    vq = np.zeros((r, d), dtype=np.int64)
+    cq = np.zeros((P, r), dtype=np.int64)
+    sv = np.zeros(r)
+    sc = np.zeros(r)
+    for j in range(r):
+        vq[j], sv[j] = quantize_symmetric(V[:, j], INT4_MAX)
+        cq[:, j], sc[j] = quantize_symmetric(C[:, j], INT8_MAX)
+    muq, smu = quantize_symmetric(mu, INT8_MAX)
+    return dict(vq=vq, sv=sv, cq=cq, sc=sc, muq=muq, smu=smu)
+
+
+def dequantize_summary(qs: dict):
+    """The summary a quantised one stands for: (V d x r, C P x r, mu d)."""
+    V = (qs["vq"] * qs["sv"][:, None]).T.astype(np.float64)
+    C = (qs["cq"] * qs["sc"][None, :]).astype(np.float64)
+    mu = (qs["muq"] * qs["smu"]).astype(np.float64)
+    return V, C, mu
+
+
+def quantized_page_summary(K: np.ndarray, r: int) -> dict:
+    """Centred rank-r summary of a page-head, quantised ([expl] §2: centred
+    keys, then int4 basis and int8 coefficients / centroid)."""
+    V, C, mu, _ = page_summary(K, r, centered=True)
+    return quantize_summary(V, C, mu)
 
 
 # ---------------------------------------------------------------------------

@@ -78,7 +78,20 @@ def _attention_no_scale(q, K, V, scale=None):
     return ORIG["attention"](q, K, V, 1.0)
 
 
-ORIG = {n: getattr(L, n) for n in ("page_summary", "attention")}
+def _quant_floor(x, qmax):
+    x = np.asarray(x, dtype=np.float64)
+    amax = float(np.max(np.abs(x))) if x.size else 0.0
+    s = float(np.float32(amax / qmax)) if amax > 0 else 0.0
+    if s == 0.0:
+        return np.zeros(x.shape, dtype=np.int64), 0.0
+    return np.clip(np.floor(x / s), -qmax, qmax).astype(np.int64), s
+
+
+def _quant_wide_scale(x, qmax):
+    return ORIG["quantize_symmetric"](x, qmax + 1)
+
+
+ORIG = {n: getattr(L, n) for n in ("page_summary", "attention", "quantize_symmetric")}
 
 MUTANTS = {
     "lse_without_max_shift": ("logsumexp", _lse_no_shift),
@@ -90,6 +103,8 @@ MUTANTS = {
     "summary_coefficients_without_sigma": ("page_summary", _summary_no_sigma),
     "summary_smallest_singular_vectors": ("page_summary", _summary_smallest),
     "attention_without_scale": ("attention", _attention_no_scale),
+    "quantize_truncates": ("quantize_symmetric", _quant_floor),
+    "quantize_scale_one_code_too_wide": ("quantize_symmetric", _quant_wide_scale),
 }
 
 PIN_TESTS = [
@@ -103,6 +118,9 @@ PIN_TESTS = [
     pins.test_topk_ties_go_to_lower_index_and_sorted,
     pins.test_attention_closed_form_weights,
     pins.test_summary_transpose_slip_detected,
+    pins.test_quantize_roundtrip_within_half_step,
+    pins.test_quantize_exact_on_its_grid,
+    pins.test_quantized_summary_dequantizes_to_the_summary,
 ]
 
 

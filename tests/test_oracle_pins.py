@@ -358,3 +358,54 @@ def test_generator_poison_never_read():
     assert np.isnan(bf16_to_f32(case.k_pool)).any()
     od, _ = O.dense_decode(case.q, case.k_pool, case.v_pool, case.block_table, case.seq_lens, 2)
     assert np.isfinite(od).all()
+
+
+# --- quantised summary ------------------------------------------------------
+
+def test_quantize_roundtrip_within_half_step():
+    """Quantised storage (explainer §2 'Implementatie': int4 basis, int8
+    coefficients and centroid), symmetric per-vector scales: every value is
+    recovered to within half a quantisation step, the largest magnitude maps
+    to +-qmax, and every code lies in [-qmax, qmax]."""
+    rng = np.random.default_rng(11)
+    for qmax in (O.INT4_MAX, O.INT8_MAX):
+        for n in (8, 64, 128):
+            x = rng.standard_normal(n) * rng.uniform(0.01, 20.0)
+            q, s = O.quantize_symmetric(x, qmax)
+            assert s > 0 and np.all(np.abs(q) <= qmax)
+            assert np.all(np.abs(q * s - x) <= s / 2 * (1 + 1e-9))
+            i = int(np.argmax(np.abs(x)))
+            assert abs(q[i]) == qmax and np.sign(q[i]) == np.sign(x[i])
+
+
+def test_quantize_exact_on_its_grid():
+    """Values already on a scale's grid (integers times a float32 scale, one of
+    them at +-qmax) come back unchanged, with that scale."""
+    rng = np.random.default_rng(12)
+    for qmax in (O.INT4_MAX, O.INT8_MAX):
+        ints = rng.integers(-qmax, qmax + 1, size=64)
+        ints[5] = -qmax
+        s0 = float(np.float32(0.0371))
+        q, s = O.quantize_symmetric(ints * s0, qmax)
+        assert s == s0 and np.array_equal(q, ints)
+    q, s = O.quantize_symmetric(np.zeros(16), O.INT4_MAX)
+    assert s == 0.0 and not q.any()
+
+
+def test_quantized_summary_dequantizes_to_the_summary():
+    """dequantize(quantize(V, C, mu)) is (V, C, mu) to within half a step of
+    each vector's scale, column by column (a transposed layout or a scale
+    applied to the wrong axis breaks this), and its page LSE follows the
+    centred equation for s_hat_j(q)."""
+    rng = np.random.default_rng(13)
+    K = rng.standard_normal((64, 128)) + 0.5
+    V, C, mu, _ = O.page_summary(K, 6, centered=True)
+    qs = O.quantize_summary(V, C, mu)
+    V2, C2, mu2 = O.dequantize_summary(qs)
+    assert V2.shape == V.shape and C2.shape == C.shape
+    assert np.all(np.abs(V2 - V) <= qs["sv"][None, :] / 2 * (1 + 1e-9))
+    assert np.all(np.abs(C2 - C) <= qs["sc"][None, :] / 2 * (1 + 1e-9))
+    assert np.all(np.abs(mu2 - mu) <= qs["smu"] / 2 * (1 + 1e-9))
+    q = rng.standard_normal(128)
+    direct = math.log(math.fsum(math.exp(v) for v in (C2 @ V2.T @ q + q @ mu2) / math.sqrt(128)))
+    assert abs(O.reconstructed_page_lse(q, V2, C2, mu2) - direct) < 1e-12
