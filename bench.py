@@ -424,6 +424,49 @@ def run_gpu(args):
                     kept += int(cpg) in cs
     assert rt.device_error() == 0
 
+    # The quantised, centred summary format (int4 basis, int8 coefficients and
+    # centroid) on the same caches: its builder, step and scan.
+    q4 = None
+    if r <= 8 and not args.no_q4:
+        from sparse_kv_page_rank_gb300.locks import q4_page_head_bytes
+        qrts = [LocksRuntime(rt_.k_pool, rt_.v_pool, bt, sl, ns, Hq, r, budget, quantized=True) for rt_ in rts]
+        torch.cuda.synchronize()
+        e0.record()
+        qrts[0].build_summaries(pages)
+        e1.record()
+        torch.cuda.synchronize()
+        q4_build_ms = e0.elapsed_time(e1)
+        for qrt in qrts[1:]:
+            qrt.set_summaries(qrts[0].basis_t, None)
+        q4_step_ms = timed(lambda i, rt_: qrts[i].decode_step(q, stream=stream), K, W)
+        q4_scan_ms = timed(lambda i, rt_: qrts[i].page_scores(q, page_lse_bufs[i], stream=stream), K, W)
+        qerrs = [qrt.device_error() for qrt in qrts]
+        if any(qerrs):
+            raise SystemExit(f"device error bits {qerrs} after the quantised-format steps: this run is invalid")
+        qrts[0].decode_step(q)
+        torch.cuda.synchronize()
+        qsel = qrts[0].sel_pages.cpu().numpy()
+        qcnt = qrts[0].sel_count.cpu().numpy()
+        qrec, qkept = [], 0
+        for b in range(B):
+            n = int(nsum_host[b])
+            for h in range(Hkv):
+                s_star = ex[b, h * G:(h + 1) * G, :n]
+                tot = np.logaddexp.reduce(s_star, axis=1)
+                chosen = qsel[b, h, :qcnt[b, h]]
+                qrec.append(float(np.mean(np.exp(np.logaddexp.reduce(s_star[:, chosen], axis=1) - tot))))
+                cs = set(chosen.tolist())
+                qkept += sum(int(cpg) in cs for cpg in case.carriers[b, h] if cpg >= 0)
+        qb = q4_page_head_bytes(r)
+        q_scan_alg = Hkv * int(nsum_host.sum()) * (qb + G * 4)
+        q4 = {"value": q4_step_ms * 1e3, "unit": "us", "summary_bytes_per_page_head": qb,
+              "residency": qb / (2 * P * D * 2), "speedup_vs_dense": dense_ms / q4_step_ms,
+              "scan_us": q4_scan_ms * 1e3, "scan_gbs": q_scan_alg / (q4_scan_ms * 1e-3) / 1e9,
+              "mass_recall": float(np.mean(qrec)), "carrier_retention": qkept / total if total else None,
+              "summary_build": {"pages_per_s": pages.numel() * Hkv / (q4_build_ms / 1e3), "ms": q4_build_ms},
+              "format": "centred; int4 basis, int8 coefficients and centroid, float32 scales per vector"}
+        del qrts
+
     n_sum_tot = int(nsum_host.sum())
     sb = dict(summaries=0, shat=0, selected_kv=0, qo=0, total=0)
     for b in range(B):
@@ -478,6 +521,7 @@ def run_gpu(args):
                 "d2h_bytes_per_step": int(B * Hq * D * 2),
                 "how": "per step inside one CUDA graph: cudaMemcpyAsync pinned q -> device, "
                        "locks_decode_step, out -> pinned host"},
+        "q4": q4,
         "gpu_launches": 3 * K,
         "clocks": clk,
     }
@@ -498,6 +542,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--copies", type=int, default=0, help="independent cache copies to rotate (0 = auto)")
     ap.add_argument("--profile", action="store_true", help="only replay the step, dense and scan graphs")
+    ap.add_argument("--no-q4", action="store_true", help="skip the quantised summary format's measurements")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

@@ -81,6 +81,12 @@ typedef enum {
 
 #define LOCKS_DTYPE_BF16 0
 #define LOCKS_DTYPE_F32 1
+#define LOCKS_DTYPE_Q4 2
+
+/* Bytes of one page-head of a LOCKS_DTYPE_Q4 summary at rank r (head_dim 128,
+ * page_size 64): 64r basis + 128 centroid + 64r coefficients + 4(2r+1) scales,
+ * rounded up to 16. */
+#define LOCKS_Q4_PAGE_HEAD_BYTES(r) ((((136 * (r)) + 132) + 15) / 16 * 16)
 
 /* Paged KV cache.  K and V pools hold whole pages for all KV heads:
  *   k_pool, v_pool  bf16 [pages_total][num_kv_heads][page_size][head_dim]
@@ -113,7 +119,22 @@ typedef struct locks_cache {
  *   coeffs   [pages_total][num_kv_heads][page_size][rank]: row i is c_i
  *   dtype    LOCKS_DTYPE_BF16 for everything that reads summaries;
  *            LOCKS_DTYPE_F32 is accepted by locks_build_summaries only (a
- *            full-precision copy for validation). */
+ *            full-precision copy for validation);
+ *            LOCKS_DTYPE_Q4: the quantised, centred format of the explainer's
+ *            §2 "Implementatie" (int4 basis, int8 coefficients and centroid),
+ *            rank 2..8.  Then basis_t points to one block of
+ *            LOCKS_Q4_PAGE_HEAD_BYTES(rank) bytes per page-head,
+ *            [pages_total][num_kv_heads][bytes], and coeffs is unused:
+ *              byte 0       basis: row j (j < rank) at 64 j, element t at
+ *                           64 j + t/2, low nibble for even t, two's complement
+ *                           codes in [-7, 7]
+ *              byte 64r     centroid mu: 128 int8 codes in [-127, 127]
+ *              byte 64r+128 coefficients: int8 codes [page_size][rank]
+ *              byte 128r+128 float32 scales: basis s_v[rank], coefficients
+ *                           s_c[rank], centroid s_mu
+ *            The summary stands for V_j = s_v[j] * code, c_i[j] = s_c[j] *
+ *            code, mu = s_mu * code, and the page's keys are approximated
+ *            by mu + sum_j c_i[j] V_j (centred). */
 typedef struct locks_summary {
   void* basis_t;
   void* coeffs;

@@ -68,11 +68,14 @@ locks_status_t check_params(const locks_cache_t* c, const locks_params_t* p) {
 }
 
 locks_status_t check_summary(const locks_summary_t* s, bool for_scan) {
-  if (!s || !s->basis_t || !s->coeffs) return LOCKS_ERR_INVALID_ARG;
+  if (!s || !s->basis_t) return LOCKS_ERR_INVALID_ARG;
+  const bool q4 = s->dtype == LOCKS_DTYPE_Q4;  // one packed array; coeffs unused
+  if (!q4 && !s->coeffs) return LOCKS_ERR_INVALID_ARG;
   if (s->rank < 2 || s->rank > 16 || (s->rank & 1)) return LOCKS_ERR_UNSUPPORTED;
-  if (s->dtype != LOCKS_DTYPE_BF16 && s->dtype != LOCKS_DTYPE_F32) return LOCKS_ERR_INVALID_ARG;
-  if (for_scan && s->dtype != LOCKS_DTYPE_BF16) return LOCKS_ERR_UNSUPPORTED;
-  if ((reinterpret_cast<uintptr_t>(s->basis_t) | reinterpret_cast<uintptr_t>(s->coeffs)) & 15)
+  if (s->dtype != LOCKS_DTYPE_BF16 && s->dtype != LOCKS_DTYPE_F32 && !q4) return LOCKS_ERR_INVALID_ARG;
+  if (q4 && s->rank > 8) return LOCKS_ERR_UNSUPPORTED;
+  if (for_scan && s->dtype == LOCKS_DTYPE_F32) return LOCKS_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(s->basis_t) | (q4 ? 0 : reinterpret_cast<uintptr_t>(s->coeffs))) & 15)
     return LOCKS_ERR_INVALID_ARG;
   return LOCKS_OK;
 }
@@ -237,6 +240,7 @@ locks_status_t run_select(const locks_cache_t* c, const locks_summary_t* s, cons
   sa.chunk_pages = pl.scan_chunk;
   sa.n_chunks = pl.n_scan;
   sa.scale_log2 = scale_of(p) * kLog2e;
+  sa.q4 = s->dtype == LOCKS_DTYPE_Q4 ? 1 : 0;
   cudaError_t e = launch_scan(sa, st, true);
   if (e != cudaSuccess) return LOCKS_ERR_CUDA;
   if (!sel) return LOCKS_OK;  // scan only
@@ -361,7 +365,7 @@ locks_status_t locks_build_summaries(const locks_cache_t* cache, locks_summary_t
   a.num_kv_heads = cache->num_kv_heads;
   a.rank = summary->rank;
   a.pages_total = cache->pages_total;
-  a.out_f32 = summary->dtype == LOCKS_DTYPE_F32;
+  a.format = summary->dtype;
   a.err = ws ? static_cast<int*>(ws) : nullptr;  // the error word is at offset 0 of every workspace
   return cuda_status(launch_build(a, static_cast<cudaStream_t>(stream)));
 }

@@ -22,6 +22,16 @@
 //      coefficient matrix for the computed basis in any case.
 // Output: basis_t [r][d] (rows = basis vectors, descending singular value)
 // and coeffs [P][r], bf16 or fp32.
+//
+// Quantised format (explainer §2 "Implementatie": centred keys, int4 basis,
+// int8 coefficients and centroid): the same steps on the centred keys
+// K~ = K - 1 mu^T (mu = mean key of the page).  The Gram matrix of K~ is A
+// with its row and column means removed (A~_ij = A_ij - m_i - m_j + m, m_i
+// the row means of A and m their mean), so the tensor-core product is kept;
+// V = K~^T U_r = K^T U_r - mu (1^T U_r) and C = K~ V = K V - 1 (mu^T V).
+// Each basis vector, coefficient column and the centroid then get one
+// symmetric float32 scale s = max|x| / qmax (qmax 7 for int4, 127 for int8)
+// and codes rint(x / s), packed as LOCKS_Q4_PAGE_HEAD_BYTES(r) bytes.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -51,6 +61,12 @@ struct BuildSmem {
   int pp[kLmax / 2][2];     // pair members of the current round
   int order[kLmax];
   float red[kBW];
+  // quantised format only
+  float mu[kHeadDim];  // mean key
+  float rm[kPage];     // row means of A
+  float cs[16];        // column sums of U_r, then mu . V_j
+  float sv[16], sc[16], smu;
+  float grand;
 };
 
 // Y = A X  (64 x l); A symmetric 64 x 64
@@ -110,6 +126,15 @@ __global__ void __launch_bounds__(kBT) build_kernel(const BuildArgs a) {
     const int row = e / 16, col = (e % 16) * 8;
     *reinterpret_cast<uint4*>(&s.K[row * kKS + col]) = __ldg(reinterpret_cast<const uint4*>(kg + row * kHeadDim + col));
   }
+  const bool q4 = a.format == LOCKS_DTYPE_Q4;
+  if (q4) {
+    __syncthreads();  // K is in shared memory
+    for (int dd = tid; dd < kHeadDim; dd += kBT) {
+      float acc = 0.f;
+      for (int i = 0; i < kPage; ++i) acc += __bfloat162float(__ushort_as_bfloat16(s.K[i * kKS + dd]));
+      s.mu[dd] = acc * (1.f / kPage);
+    }
+  }
   __syncthreads();
 
   // 1. A = K K^T : warp w -> rows 16*(w/2).., columns 32*(w%2)..
@@ -147,6 +172,26 @@ __global__ void __launch_bounds__(kBT) build_kernel(const BuildArgs a) {
     }
   }
   __syncthreads();
+  if (q4) {
+    // Gram matrix of the centred keys: remove the row and column means
+    for (int i = tid; i < kPage; i += kBT) {
+      float acc = 0.f;
+      for (int j = 0; j < kPage; ++j) acc += s.A[i * kAS + j];
+      s.rm[i] = acc * (1.f / kPage);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      float acc = 0.f;
+      for (int i = 0; i < kPage; ++i) acc += s.rm[i];
+      s.grand = acc * (1.f / kPage);
+    }
+    __syncthreads();
+    for (int e = tid; e < kPage * kPage; e += kBT) {
+      const int i = e / kPage, j = e % kPage;
+      s.A[i * kAS + j] = s.A[i * kAS + j] - s.rm[i] - s.rm[j] + s.grand;
+    }
+    __syncthreads();
+  }
 
   // 2. subspace iteration.  Start: A * (fixed +-1 pattern).
   for (int e = tid; e < kPage * l; e += kBT) {
@@ -273,12 +318,22 @@ __global__ void __launch_bounds__(kBT) build_kernel(const BuildArgs a) {
   }
   __syncthreads();
 
-  // 4. V = K^T U_r  (d x r) into s.V as rows [j][d]
+  // 4. V = K^T U_r  (d x r) into s.V as rows [j][d] (centred: minus mu 1^T U_r)
+  if (q4) {
+    for (int j = warp; j < r; j += kBW) {
+      float acc = 0.f;
+      for (int i = lane; i < kPage; i += 32) acc += s.Y[i * kXS + j];
+      acc = warp_sum(acc);
+      if (lane == 0) s.cs[j] = acc;
+    }
+    __syncthreads();
+  }
   for (int e = tid; e < kHeadDim * r; e += kBT) {
     const int dd = e % kHeadDim, j = e / kHeadDim;
     float acc = 0.f;
     for (int i = 0; i < kPage; ++i)
       acc = fmaf(__bfloat162float(__ushort_as_bfloat16(s.K[i * kKS + dd])), s.Y[i * kXS + j], acc);
+    if (q4) acc -= s.mu[dd] * s.cs[j];
     s.V[j * kVS + dd] = acc;
   }
   __syncthreads();
@@ -306,18 +361,65 @@ __global__ void __launch_bounds__(kBT) build_kernel(const BuildArgs a) {
     }
   }
 
-  // C = K V  (64 x r) -> Y
+  // C = K V  (64 x r) -> Y  (centred: minus mu . V_j)
+  if (q4) {
+    for (int j = warp; j < r; j += kBW) {
+      float acc = 0.f;
+      for (int k = lane; k < kHeadDim; k += 32) acc = fmaf(s.mu[k], s.V[j * kVS + k], acc);
+      acc = warp_sum(acc);
+      if (lane == 0) s.cs[j] = acc;
+    }
+    __syncthreads();
+  }
   for (int e = tid; e < kPage * r; e += kBT) {
     const int i = e / r, j = e % r;
     float acc = 0.f;
     for (int k = 0; k < kHeadDim; ++k)
       acc = fmaf(__bfloat162float(__ushort_as_bfloat16(s.K[i * kKS + k])), s.V[j * kVS + k], acc);
+    if (q4) acc -= s.cs[j];
     s.Y[i * kXS + j] = acc;
   }
   __syncthreads();
 
   // store
-  if (a.out_f32) {
+  if (q4) {
+    // one symmetric scale per basis vector (int4), per coefficient column
+    // and for the centroid (int8)
+    for (int j = warp; j <= r; j += kBW) {
+      float av = 0.f, ac = 0.f;
+      if (j < r) {
+        for (int k = lane; k < kHeadDim; k += 32) av = fmaxf(av, fabsf(s.V[j * kVS + k]));
+        for (int i = lane; i < kPage; i += 32) ac = fmaxf(ac, fabsf(s.Y[i * kXS + j]));
+      } else {
+        for (int k = lane; k < kHeadDim; k += 32) ac = fmaxf(ac, fabsf(s.mu[k]));
+      }
+      av = warp_max(av);
+      ac = warp_max(ac);
+      if (lane == 0) {
+        if (j < r) {
+          s.sv[j] = av / 7.f;
+          s.sc[j] = ac / 127.f;
+        } else {
+          s.smu = ac / 127.f;
+        }
+      }
+    }
+    __syncthreads();
+    auto code = [](float x, float sc, float qmax) -> int {
+      return sc > 0.f ? (int)fminf(fmaxf(rintf(x / sc), -qmax), qmax) : 0;
+    };
+    uint8_t* blk = static_cast<uint8_t*>(a.basis_t) + ph * (size_t)LOCKS_Q4_PAGE_HEAD_BYTES(r);
+    for (int e = tid; e < r * (kHeadDim / 2); e += kBT) {
+      const int j = e / (kHeadDim / 2), bb = e % (kHeadDim / 2);
+      const int lo = code(s.V[j * kVS + 2 * bb], s.sv[j], 7.f), hi = code(s.V[j * kVS + 2 * bb + 1], s.sv[j], 7.f);
+      blk[e] = (uint8_t)((lo & 15) | ((hi & 15) << 4));
+    }
+    for (int k = tid; k < kHeadDim; k += kBT) blk[64 * r + k] = (uint8_t)(int8_t)code(s.mu[k], s.smu, 127.f);
+    for (int e = tid; e < kPage * r; e += kBT)
+      blk[64 * r + kHeadDim + e] = (uint8_t)(int8_t)code(s.Y[(e / r) * kXS + e % r], s.sc[e % r], 127.f);
+    float* sco = reinterpret_cast<float*>(blk + 128 * r + kHeadDim);
+    for (int e = tid; e < 2 * r + 1; e += kBT) sco[e] = e < r ? s.sv[e] : (e < 2 * r ? s.sc[e - r] : s.smu);
+  } else if (a.format == LOCKS_DTYPE_F32) {
     float* bo = reinterpret_cast<float*>(a.basis_t) + ph * (size_t)r * kHeadDim;
     float* co = reinterpret_cast<float*>(a.coeffs) + ph * (size_t)kPage * r;
     for (int e = tid; e < r * kHeadDim; e += kBT) bo[e] = s.V[(e / kHeadDim) * kVS + e % kHeadDim];

@@ -190,6 +190,28 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
+__device__ __forceinline__ uint32_t lds16(uint32_t addr) {
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];\n" : "=h"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];\n" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+// Two signed 4-bit codes (bits sh..sh+3 and sh+4..sh+7 of w) as a bf16 pair
+// (first code in the low half); small integers are exact in bf16.
+__device__ __forceinline__ uint32_t i4pair_bf16(uint32_t w, int sh) {
+  const int lo = ((int)(w << (28 - sh))) >> 28, hi = ((int)(w << (24 - sh))) >> 28;
+  return (__float_as_uint((float)lo) >> 16) | (__float_as_uint((float)hi) & 0xffff0000u);
+}
+// The two signed 8-bit codes in bytes 0 and 1 of v as a bf16 pair.
+__device__ __forceinline__ uint32_t i8pair_bf16(uint32_t v) {
+  const int lo = ((int)(v << 24)) >> 24, hi = ((int)(v << 16)) >> 24;
+  return (__float_as_uint((float)lo) >> 16) | (__float_as_uint((float)hi) & 0xffff0000u);
+}
+
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));

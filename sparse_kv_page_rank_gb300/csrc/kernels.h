@@ -22,6 +22,7 @@ struct ScanArgs {
   int batch, num_kv_heads, group, rank, max_pages, pages_total;
   int chunk_pages, n_chunks;
   float scale_log2;            // scale * log2(e)
+  int q4;                      // 1: basis_t holds LOCKS_DTYPE_Q4 blocks (coeffs unused)
 };
 
 // GSA scores + top-k (chunk-local candidates, merged by the last CTA).
@@ -73,7 +74,8 @@ struct BuildArgs {
   void* basis_t;
   void* coeffs;
   const int32_t* page_ids;
-  int n, num_kv_heads, rank, pages_total, out_f32;
+  int n, num_kv_heads, rank, pages_total;
+  int format;  // LOCKS_DTYPE_BF16 / _F32 (basis_t + coeffs) or _Q4 (packed blocks in basis_t)
   int* err;
 };
 

@@ -48,16 +48,17 @@ namespace {
 // order.  (With a slot shared by several warps, a warp could wait on the
 // parity of a slot's next phase while the current one is still incomplete;
 // a parity wait on a phase two ahead returns at once, on stale data.)
-template <bool R16>
+template <bool R16, bool Q4 = false>
 struct Ring {
   static constexpr int kSlots = R16 ? 2 * kScanWarps : 4 * kScanWarps;  // page-heads in flight per CTA
   static constexpr int kCoef = R16 ? 4096 : 2048;  // basis block (r rows x 256 B) comes first
-  static constexpr int kSlot = R16 ? 6144 : 3072;
+  // quantised: one packed block per page-head (rank <= 8)
+  static constexpr int kSlot = Q4 ? LOCKS_Q4_PAGE_HEAD_BYTES(8) : (R16 ? 6144 : 3072);
 };
 
-template <bool R16>
+template <bool R16, bool Q4 = false>
 constexpr int scan_smem_bytes() {
-  return Ring<R16>::kSlots * Ring<R16>::kSlot + 1024;
+  return Ring<R16, Q4>::kSlots * Ring<R16, Q4>::kSlot + 1024;
 }
 
 // x -> hi + mid + lo, each term a bf16 (truncated; the three keep about 21
@@ -230,9 +231,107 @@ __device__ __forceinline__ void compute_page(uint32_t slot, const uint4 (&qa)[4]
   }
 }
 
-template <bool G16, bool R16, bool GRP2>
+// The same page-head estimate from the quantised, centred format (int4 basis
+// codes, int8 centroid and coefficient codes, float32 scales; rank <= 8):
+// the codes are exact in bf16, so the contractions run on them directly and
+// the scales enter in fp32 -- each basis vector's and coefficient column's
+// scale on its column of W, the centroid's on q . mu, which shifts every
+// logit of the head alike and is added to the page's LSE.
+template <bool G16, bool GRP2>
+__device__ __forceinline__ void compute_page_q4(uint32_t slot, const uint4 (&qa)[4], const uint4 (&qb)[4], int r,
+                                                float scale_log2, int lane, float& e0, float& e1) {
+  const int g = lane >> 2, c = lane & 3;
+  const uint32_t mu_off = 64 * r, coef_off = 64 * r + kHeadDim, sc_off = 128 * r + kHeadDim;
+  // (1) W^T = Q V (basis codes) and, as column 0 of a second tile, Q mu
+  float w0[4] = {0.f, 0.f, 0.f, 0.f}, x0[4] = {0.f, 0.f, 0.f, 0.f};
+  float u0[4] = {0.f, 0.f, 0.f, 0.f}, y0[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    // elements 32s + 8c .. +7 of basis row g: 4 bytes of nibbles
+    const uint32_t nib = (g < r) ? lds32(slot + 64 * g + 16 * s + 4 * c) : 0u;
+    mma_16816(w0, qa[s].x, qb[s].x, qa[s].y, qb[s].y, i4pair_bf16(nib, 0), i4pair_bf16(nib, 8));
+    mma_16816(x0, qa[s].z, qb[s].z, qa[s].w, qb[s].w, i4pair_bf16(nib, 16), i4pair_bf16(nib, 24));
+    const uint2 m8 = (g == 0) ? lds64(slot + mu_off + 32 * s + 8 * c) : make_uint2(0u, 0u);
+    mma_16816(u0, qa[s].x, qb[s].x, qa[s].y, qb[s].y, i8pair_bf16(m8.x), i8pair_bf16(m8.x >> 16));
+    mma_16816(y0, qa[s].z, qb[s].z, qa[s].w, qb[s].w, i8pair_bf16(m8.y), i8pair_bf16(m8.y >> 16));
+  }
+  // column j of W gets s_v[j] * s_c[j] (and the base-2 logit scale)
+  const int j0 = 2 * c, j1 = 2 * c + 1;
+  const float f0 = j0 < r ? __uint_as_float(lds32(slot + sc_off + 4 * j0)) *
+                                __uint_as_float(lds32(slot + sc_off + 4 * (r + j0))) * scale_log2
+                          : 0.f;
+  const float f1 = j1 < r ? __uint_as_float(lds32(slot + sc_off + 4 * j1)) *
+                                __uint_as_float(lds32(slot + sc_off + 4 * (r + j1))) * scale_log2
+                          : 0.f;
+  const float fmu = __uint_as_float(lds32(slot + sc_off + 8 * r)) * scale_log2;
+  // q . mu of this lane's head rows, held by lane (g, 0)
+  const float qmu0 = __shfl_sync(0xffffffffu, (u0[0] + y0[0]) * fmu, lane & ~3);
+  const float qmu1 = __shfl_sync(0xffffffffu, (u0[2] + y0[2]) * fmu, lane & ~3);
+  const float wa = (w0[0] + x0[0]) * f0, wb = (w0[1] + x0[1]) * f1;
+  const float wc = (w0[2] + x0[2]) * f0, wd = (w0[3] + x0[3]) * f1;
+  auto coef = [&](int jt) -> uint32_t {
+    return (2 * c < r) ? i8pair_bf16(lds16(slot + coef_off + (8 * jt + g) * r + 2 * c)) : 0u;
+  };
+
+  if (GRP2) {
+    uint32_t hh, mm, ll;
+    split3(wa, wb, hh, mm, ll);
+    const bool lo_half = lane < 16;
+    const uint32_t ha0 = lo_half ? hh : 0u, ha2 = lo_half ? 0u : hh;
+    const uint32_t ma0 = lo_half ? mm : 0u, ma2 = lo_half ? 0u : mm;
+    const uint32_t la0 = lo_half ? ll : 0u, la2 = lo_half ? 0u : ll;
+    uint32_t cbv[8];
+#pragma unroll
+    for (int jt = 0; jt < 8; ++jt) cbv[jt] = coef(jt);
+    float d[4][4];
+#pragma unroll
+    for (int jt = 0; jt < 4; ++jt) {
+      d[jt][0] = d[jt][1] = d[jt][2] = d[jt][3] = 0.f;
+      mma_16816(d[jt], la0, 0u, la2, 0u, cbv[2 * jt], cbv[2 * jt + 1]);
+      mma_16816(d[jt], ma0, 0u, ma2, 0u, cbv[2 * jt], cbv[2 * jt + 1]);
+      mma_16816(d[jt], ha0, 0u, ha2, 0u, cbv[2 * jt], cbv[2 * jt + 1]);
+    }
+    float v[8] = {d[0][0], d[0][1], d[1][0], d[1][1], d[2][0], d[2][1], d[3][0], d[3][1]};
+    e0 = lse2_lanes<8, 1, 2, 16>(v) + qmu0;
+    e1 = 0.f;
+    return;
+  }
+
+  uint32_t h0, m0, l0, h1, m1, l1;
+  split3(wa, wb, h0, m0, l0);
+  split3(wc, wd, h1, m1, l1);
+  uint32_t cb[8];
+#pragma unroll
+  for (int jt = 0; jt < 8; ++jt) cb[jt] = coef(jt);
+  float d[8][4];
+#pragma unroll
+  for (int jt = 0; jt < 8; ++jt) {
+    d[jt][0] = d[jt][1] = d[jt][2] = d[jt][3] = 0.f;
+    mma_1688(d[jt], l0, l1, cb[jt]);
+    mma_1688(d[jt], m0, m1, cb[jt]);
+    mma_1688(d[jt], h0, h1, cb[jt]);
+  }
+  float v[16];
+#pragma unroll
+  for (int jt = 0; jt < 8; ++jt) {
+    v[2 * jt] = d[jt][0];
+    v[2 * jt + 1] = d[jt][1];
+  }
+  e0 = lse2_lanes<16, 1, 2, 0>(v) + qmu0;
+  e1 = 0.f;
+  if (G16) {
+#pragma unroll
+    for (int jt = 0; jt < 8; ++jt) {
+      v[2 * jt] = d[jt][2];
+      v[2 * jt + 1] = d[jt][3];
+    }
+    e1 = lse2_lanes<16, 1, 2, 0>(v) + qmu1;
+  }
+}
+
+template <bool G16, bool R16, bool GRP2, bool Q4>
 __global__ void __launch_bounds__(kScanThreads, 2) scan_kernel(const ScanArgs a) {
-  using RG = Ring<R16>;
+  using RG = Ring<R16, Q4>;
   constexpr int S = RG::kSlots;
   static_assert(S <= 32 && S % kScanWarps == 0, "one producer lane per slot; one consumer warp per slot");
   extern __shared__ uint8_t ring_raw[];
@@ -309,9 +408,16 @@ __global__ void __launch_bounds__(kScanThreads, 2) scan_kernel(const ScanArgs a)
         if (valid) {
           const size_t ph = (size_t)phys * a.num_kv_heads + hkv;
           const uint32_t slot = ring + lane * RG::kSlot;
-          mbar_arrive_expect_tx(&full_bar[lane], basis_bytes + coef_bytes);
-          bulk_load(slot, a.basis_t + ph * ph_stride_b, basis_bytes, &full_bar[lane]);
-          bulk_load(slot + RG::kCoef, a.coeffs + ph * ph_stride_c, coef_bytes, &full_bar[lane]);
+          if (Q4) {
+            // one packed block per page-head
+            const uint32_t qbytes = (uint32_t)LOCKS_Q4_PAGE_HEAD_BYTES(r);
+            mbar_arrive_expect_tx(&full_bar[lane], qbytes);
+            bulk_load(slot, reinterpret_cast<const uint8_t*>(a.basis_t) + ph * qbytes, qbytes, &full_bar[lane]);
+          } else {
+            mbar_arrive_expect_tx(&full_bar[lane], basis_bytes + coef_bytes);
+            bulk_load(slot, a.basis_t + ph * ph_stride_b, basis_bytes, &full_bar[lane]);
+            bulk_load(slot + RG::kCoef, a.coeffs + ph * ph_stride_c, coef_bytes, &full_bar[lane]);
+          }
         } else {
           mbar_arrive(&full_bar[lane]);
         }
@@ -350,7 +456,12 @@ __global__ void __launch_bounds__(kScanThreads, 2) scan_kernel(const ScanArgs a)
       }
       const int valid = slot_ok[s];
       float e0 = 0.f, e1 = 0.f;
-      if (valid) compute_page<G16, R16, GRP2>(ring + s * RG::kSlot, qa, qb, r, a.scale_log2, lane, e0, e1);
+      if (valid) {
+        if (Q4)
+          compute_page_q4<G16, GRP2>(ring + s * RG::kSlot, qa, qb, r, a.scale_log2, lane, e0, e1);
+        else
+          compute_page<G16, R16, GRP2>(ring + s * RG::kSlot, qa, qb, r, a.scale_log2, lane, e0, e1);
+      }
       __syncwarp();  // every lane is done with the slot
       if (lane == 0) mbar_arrive(&empty_bar[s]);
       cyc_wait += t1 - t0;
@@ -397,11 +508,11 @@ __global__ void __launch_bounds__(kScanThreads, 2) scan_kernel(const ScanArgs a)
   trace_mark(a.err, kTrScanExit, false);
 }
 
-template <bool G16, bool R16, bool GRP2>
+template <bool G16, bool R16, bool GRP2, bool Q4 = false>
 cudaError_t launch_one(const ScanArgs& a, cudaStream_t s, bool pdl) {
-  const int smem = scan_smem_bytes<R16>();
+  const int smem = scan_smem_bytes<R16, Q4>();
   cudaError_t e =
-      cudaFuncSetAttribute(scan_kernel<G16, R16, GRP2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      cudaFuncSetAttribute(scan_kernel<G16, R16, GRP2, Q4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_chunks, a.batch * a.num_kv_heads, 1);
@@ -413,13 +524,18 @@ cudaError_t launch_one(const ScanArgs& a, cudaStream_t s, bool pdl) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, scan_kernel<G16, R16, GRP2>, a);
+  return cudaLaunchKernelEx(&cfg, scan_kernel<G16, R16, GRP2, Q4>, a);
 }
 
 }  // namespace
 
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s, bool pdl) {
   const bool g16 = a.group > 8, r16 = a.rank > 8;
+  if (a.q4) {  // rank <= 8 (checked by the caller)
+    if (g16) return launch_one<true, false, false, true>(a, s, pdl);
+    if (a.group <= 4) return launch_one<false, false, true, true>(a, s, pdl);
+    return launch_one<false, false, false, true>(a, s, pdl);
+  }
   if (g16) return r16 ? launch_one<true, true, false>(a, s, pdl) : launch_one<true, false, false>(a, s, pdl);
   if (r16) return launch_one<false, true, false>(a, s, pdl);
   if (a.group <= 4) return launch_one<false, false, true>(a, s, pdl);

@@ -17,12 +17,14 @@ class LocksRuntime:
 
     k_pool, v_pool: bf16 [pages_total][Hkv][64][128]; block_table int32
     [B][max_pages]; seq_lens, n_summarized int32 [B].  Summaries are
-    allocated here (bf16 [pages_total][Hkv][rank][128] and [..][64][rank]).
+    allocated here: bf16 [pages_total][Hkv][rank][128] and [..][64][rank],
+    or, with ``quantized``, one packed LOCKS_DTYPE_Q4 block per page-head
+    (uint8 [pages_total][Hkv][q4_page_head_bytes(rank)]).
     """
 
     def __init__(self, k_pool: torch.Tensor, v_pool: torch.Tensor, block_table: torch.Tensor,
                  seq_lens: torch.Tensor, n_summarized: torch.Tensor, num_q_heads: int, rank: int,
-                 budget_tokens: int, scale: float = 0.0):
+                 budget_tokens: int, scale: float = 0.0, quantized: bool = False):
         assert k_pool.dtype == torch.bfloat16 and v_pool.dtype == torch.bfloat16
         assert block_table.dtype == torch.int32 and seq_lens.dtype == torch.int32
         self.device = k_pool.device
@@ -33,10 +35,16 @@ class LocksRuntime:
         self.batch = block_table.shape[0]
         self.num_kv_heads, self.num_q_heads = hkv, num_q_heads
         self.rank = rank
-        self.basis_t = torch.zeros((pt, hkv, rank, d), dtype=torch.bfloat16, device=self.device)
-        self.coeffs = torch.zeros((pt, hkv, P, rank), dtype=torch.bfloat16, device=self.device)
+        self.quantized = quantized
+        if quantized:
+            self.basis_t = torch.zeros((pt, hkv, L.q4_page_head_bytes(rank)), dtype=torch.uint8, device=self.device)
+            self.coeffs = None
+        else:
+            self.basis_t = torch.zeros((pt, hkv, rank, d), dtype=torch.bfloat16, device=self.device)
+            self.coeffs = torch.zeros((pt, hkv, P, rank), dtype=torch.bfloat16, device=self.device)
         self.cache = L.make_cache(k_pool, v_pool, block_table, seq_lens, self.n_summarized)
-        self.summary = L.make_summary(self.basis_t, self.coeffs, rank)
+        self.summary = L.make_summary(self.basis_t, self.coeffs, rank,
+                                      L.LOCKS_DTYPE_Q4 if quantized else L.LOCKS_DTYPE_BF16)
         self.params = L.make_params(num_q_heads, budget_tokens, scale)
         self.k_max = min(budget_tokens // P, block_table.shape[1])
         self.ws_bytes = L.locks_workspace_size(self.cache, self.summary, self.params)
@@ -50,10 +58,12 @@ class LocksRuntime:
         self.out = torch.zeros((B, num_q_heads, d), dtype=torch.bfloat16, device=self.device)
         self.lse = torch.zeros((B, num_q_heads), dtype=torch.float32, device=self.device)
 
-    def set_summaries(self, basis_t: torch.Tensor, coeffs: torch.Tensor):
-        """Install externally computed summaries (same layouts)."""
+    def set_summaries(self, basis_t: torch.Tensor, coeffs: torch.Tensor | None):
+        """Install externally computed summaries (same layouts; coeffs is
+        None for the quantised format)."""
         self.basis_t.copy_(basis_t)
-        self.coeffs.copy_(coeffs)
+        if self.coeffs is not None:
+            self.coeffs.copy_(coeffs)
 
     def build_summaries(self, page_ids: torch.Tensor, stream=None):
         ids = page_ids.to(device=self.device, dtype=torch.int32).contiguous()

@@ -30,6 +30,57 @@ def oracle_summaries_bf16(case, r: int, pages=None):
     return basis_t, coeffs
 
 
+def pack_q4(qs: dict, r: int) -> np.ndarray:
+    """One oracle-quantised page-head summary in the LOCKS_DTYPE_Q4 byte layout."""
+    nbytes = (136 * r + 132 + 15) // 16 * 16
+    buf = np.zeros(nbytes, dtype=np.uint8)
+    nib = (np.asarray(qs["vq"]) & 15).astype(np.uint8)  # [r][128] two's-complement nibbles
+    buf[:64 * r] = (nib[:, 0::2] | (nib[:, 1::2] << 4)).reshape(-1)
+    buf[64 * r:64 * r + 128] = np.asarray(qs["muq"]).astype(np.int8).view(np.uint8)
+    buf[64 * r + 128:128 * r + 128] = np.asarray(qs["cq"]).astype(np.int8).reshape(-1).view(np.uint8)
+    scales = np.concatenate([qs["sv"], qs["sc"], [qs["smu"]]]).astype(np.float32)
+    buf[128 * r + 128:128 * r + 128 + 4 * (2 * r + 1)] = scales.view(np.uint8)
+    return buf
+
+
+def unpack_q4(buf: np.ndarray, r: int, P: int = 64, d: int = 128) -> dict:
+    """Inverse of pack_q4 (reads the ABI layout back into codes and scales)."""
+    buf = np.asarray(buf, dtype=np.uint8)
+    packed = buf[:64 * r].reshape(r, d // 2)
+    lo = (packed & 15).astype(np.int64)
+    hi = (packed >> 4).astype(np.int64)
+    vq = np.empty((r, d), dtype=np.int64)
+    vq[:, 0::2] = np.where(lo > 7, lo - 16, lo)
+    vq[:, 1::2] = np.where(hi > 7, hi - 16, hi)
+    muq = buf[64 * r:64 * r + 128].view(np.int8).astype(np.int64)
+    cq = buf[64 * r + 128:128 * r + 128].view(np.int8).astype(np.int64).reshape(P, r)
+    sc = buf[128 * r + 128:128 * r + 128 + 4 * (2 * r + 1)].view(np.float32).astype(np.float64)
+    return dict(vq=vq, sv=sc[:r], cq=cq, sc=sc[r:2 * r], muq=muq, smu=float(sc[2 * r]))
+
+
+def oracle_summaries_q4(case, r: int, heads=None, pages=None):
+    """Oracle quantised centred summaries of every full page (or the listed
+    physical pages) for the listed KV heads (default all): the packed ABI
+    array uint8 [pages_total][Hkv][bytes] and the values it stands for in the
+    oracle layout (basis [..][d][r], coeffs [..][P][r], centroid [..][d])."""
+    pt, hkv, P, d = case.k_pool.shape
+    nbytes = (136 * r + 132 + 15) // 16 * 16
+    packed = np.zeros((pt, hkv, nbytes), dtype=np.uint8)
+    basis = np.zeros((pt, hkv, d, r))
+    coeffs = np.zeros((pt, hkv, P, r))
+    cent = np.zeros((pt, hkv, d))
+    if pages is None:
+        pages = []
+        for b in range(case.batch):
+            pages.extend(int(x) for x in case.block_table[b, :case.n_full_pages(b)])
+    for p in pages:
+        for h in (range(hkv) if heads is None else heads):
+            qs = O.quantized_page_summary(O.bf16_widen(case.k_pool[p, h]), r)
+            packed[p, h] = pack_q4(qs, r)
+            basis[p, h], coeffs[p, h], cent[p, h] = O.dequantize_summary(qs)
+    return packed, basis, coeffs, cent
+
+
 def oracle_layout_from_abi(basis_t_u16, coeffs_u16):
     """ABI layout (bf16 bits) -> oracle layout float64: basis [..][d][r], coeffs [..][P][r]."""
     basis = np.swapaxes(bf16_to_f32(basis_t_u16).astype(np.float64), -1, -2)
@@ -47,7 +98,7 @@ def torch_bf16_to_u16(t):
     return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def make_runtime(case, rank: int, budget_tokens: int, n_summarized=None, device="cuda"):
+def make_runtime(case, rank: int, budget_tokens: int, n_summarized=None, device="cuda", quantized=False):
     import torch
     from sparse_kv_page_rank_gb300.runtime import LocksRuntime
     if n_summarized is None:
@@ -56,7 +107,7 @@ def make_runtime(case, rank: int, budget_tokens: int, n_summarized=None, device=
                       torch.from_numpy(case.block_table).to(device),
                       torch.from_numpy(case.seq_lens).to(device),
                       torch.tensor(np.asarray(n_summarized, dtype=np.int32)).to(device),
-                      case.num_q_heads, rank, budget_tokens)
+                      case.num_q_heads, rank, budget_tokens, quantized=quantized)
     q = to_torch_bf16(case.q, device)
     return rt, q
 
