@@ -409,14 +409,20 @@ __global__ void __launch_bounds__(kBT) build_kernel(const BuildArgs a) {
       return sc > 0.f ? (int)fminf(fmaxf(rintf(x / sc), -qmax), qmax) : 0;
     };
     uint8_t* blk = static_cast<uint8_t*>(a.basis_t) + ph * (size_t)LOCKS_Q4_PAGE_HEAD_BYTES(r);
-    for (int e = tid; e < r * (kHeadDim / 2); e += kBT) {
-      const int j = e / (kHeadDim / 2), bb = e % (kHeadDim / 2);
-      const int lo = code(s.V[j * kVS + 2 * bb], s.sv[j], 7.f), hi = code(s.V[j * kVS + 2 * bb + 1], s.sv[j], 7.f);
-      blk[e] = (uint8_t)((lo & 15) | ((hi & 15) << 4));
+    // basis: word m of row j holds elements 8m .. 8m+7, element 8m+i at
+    // bits 4(i/2) + 16(i%2), as code + 8
+    uint32_t* bw = reinterpret_cast<uint32_t*>(blk);
+    for (int e = tid; e < r * (kHeadDim / 8); e += kBT) {
+      const int j = e / (kHeadDim / 8), m = e % (kHeadDim / 8);
+      uint32_t w = 0u;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        w |= (uint32_t)(code(s.V[j * kVS + 8 * m + i], s.sv[j], 7.f) + 8) << (4 * (i / 2) + 16 * (i % 2));
+      bw[e] = w;
     }
-    for (int k = tid; k < kHeadDim; k += kBT) blk[64 * r + k] = (uint8_t)(int8_t)code(s.mu[k], s.smu, 127.f);
+    for (int k = tid; k < kHeadDim; k += kBT) blk[64 * r + k] = (uint8_t)(code(s.mu[k], s.smu, 127.f) + 128);
     for (int e = tid; e < kPage * r; e += kBT)
-      blk[64 * r + kHeadDim + e] = (uint8_t)(int8_t)code(s.Y[(e / r) * kXS + e % r], s.sc[e % r], 127.f);
+      blk[64 * r + kHeadDim + e] = (uint8_t)(code(s.Y[(e / r) * kXS + e % r], s.sc[e % r], 127.f) + 128);
     float* sco = reinterpret_cast<float*>(blk + 128 * r + kHeadDim);
     for (int e = tid; e < 2 * r + 1; e += kBT) sco[e] = e < r ? s.sv[e] : (e < 2 * r ? s.sc[e - r] : s.smu);
   } else if (a.format == LOCKS_DTYPE_F32) {

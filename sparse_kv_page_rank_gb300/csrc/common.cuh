@@ -195,21 +195,31 @@ __device__ __forceinline__ uint32_t lds16(uint32_t addr) {
   asm volatile("ld.shared.u16 %0, [%1];\n" : "=h"(v) : "r"(addr));
   return v;
 }
+__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;\n" ::"r"(addr), "r"(v) : "memory");
+}
 __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   uint2 v;
   asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];\n" : "=r"(v.x), "=r"(v.y) : "r"(addr));
   return v;
 }
-// Two signed 4-bit codes (bits sh..sh+3 and sh+4..sh+7 of w) as a bf16 pair
-// (first code in the low half); small integers are exact in bf16.
-__device__ __forceinline__ uint32_t i4pair_bf16(uint32_t w, int sh) {
-  const int lo = ((int)(w << (28 - sh))) >> 28, hi = ((int)(w << (24 - sh))) >> 28;
-  return (__float_as_uint((float)lo) >> 16) | (__float_as_uint((float)hi) & 0xffff0000u);
+// Integer codes to bf16 without int-to-float conversions: a biased code u
+// placed in the low mantissa bits of a fixed exponent is the number
+// (2^e + u) exactly, and subtracting (2^e + bias) leaves the code.
+// Two 4-bit codes stored as code + 8 in bits sh..sh+3 and sh+16..sh+19 of w:
+// bf16 (128 + u) in each half, minus 136 (all exact in bf16).
+__device__ __forceinline__ uint32_t u4pair_bf16(uint32_t w, int sh) {
+  uint32_t x = ((w >> sh) & 0x000f000fu) | 0x43004300u;
+  asm("sub.rn.bf16x2 %0, %0, %1;\n" : "+r"(x) : "r"(0x43084308u));
+  return x;
 }
-// The two signed 8-bit codes in bytes 0 and 1 of v as a bf16 pair.
-__device__ __forceinline__ uint32_t i8pair_bf16(uint32_t v) {
-  const int lo = ((int)(v << 24)) >> 24, hi = ((int)(v << 16)) >> 24;
-  return (__float_as_uint((float)lo) >> 16) | (__float_as_uint((float)hi) & 0xffff0000u);
+// Two 8-bit codes stored as code + 128 in bytes k and k+1 of w: the float
+// (2^23 + u) minus (2^23 + 128), then the two floats' upper halves (the
+// codes are small integers, exact in bf16).
+__device__ __forceinline__ uint32_t u8pair_bf16(uint32_t w, int k) {
+  const float lo = __uint_as_float(__byte_perm(w, 0x4b000000u, 0x7650u + k)) - 8388736.f;
+  const float hi = __uint_as_float(__byte_perm(w, 0x4b000000u, 0x7651u + k)) - 8388736.f;
+  return __byte_perm(__float_as_uint(lo), __float_as_uint(hi), 0x7632u);
 }
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {

@@ -56,9 +56,17 @@ struct Ring {
   static constexpr int kSlot = Q4 ? LOCKS_Q4_PAGE_HEAD_BYTES(8) : (R16 ? 6144 : 3072);
 };
 
+// Quantised format: q . mu is computed for kMuBatch pages of a warp at once
+// (one MMA tile, a page per column) instead of page by page; each warp
+// stages its pending pages' centroid codes, scales and base LSEs here.
+constexpr int kMuBatch = 8;
+constexpr int kStageMu = kScanWarps * kMuBatch * 128;        // centroid codes
+constexpr int kStageSmu = kScanWarps * kMuBatch * 4;         // centroid scales
+constexpr int kStagePend = kScanWarps * kMuBatch * 16 * 4;   // base-2 LSE per head row
+
 template <bool R16, bool Q4 = false>
 constexpr int scan_smem_bytes() {
-  return Ring<R16, Q4>::kSlots * Ring<R16, Q4>::kSlot + 1024;
+  return Ring<R16, Q4>::kSlots * Ring<R16, Q4>::kSlot + 1024 + (Q4 ? kStageMu + kStageSmu + kStagePend : 0);
 }
 
 // x -> hi + mid + lo, each term a bf16 (truncated; the three keep about 21
@@ -235,25 +243,22 @@ __device__ __forceinline__ void compute_page(uint32_t slot, const uint4 (&qa)[4]
 // codes, int8 centroid and coefficient codes, float32 scales; rank <= 8):
 // the codes are exact in bf16, so the contractions run on them directly and
 // the scales enter in fp32 -- each basis vector's and coefficient column's
-// scale on its column of W, the centroid's on q . mu, which shifts every
-// logit of the head alike and is added to the page's LSE.
+// scale on its column of W.  Returns the LSE of the centred logits; q . mu
+// shifts every logit of the head alike and is added later (mu_batch).
 template <bool G16, bool GRP2>
 __device__ __forceinline__ void compute_page_q4(uint32_t slot, const uint4 (&qa)[4], const uint4 (&qb)[4], int r,
                                                 float scale_log2, int lane, float& e0, float& e1) {
   const int g = lane >> 2, c = lane & 3;
-  const uint32_t mu_off = 64 * r, coef_off = 64 * r + kHeadDim, sc_off = 128 * r + kHeadDim;
-  // (1) W^T = Q V (basis codes) and, as column 0 of a second tile, Q mu
+  const uint32_t coef_off = 64 * r + kHeadDim, sc_off = 128 * r + kHeadDim;
+  // (1) W^T = Q V on the basis codes
   float w0[4] = {0.f, 0.f, 0.f, 0.f}, x0[4] = {0.f, 0.f, 0.f, 0.f};
-  float u0[4] = {0.f, 0.f, 0.f, 0.f}, y0[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
-    // elements 32s + 8c .. +7 of basis row g: 4 bytes of nibbles
-    const uint32_t nib = (g < r) ? lds32(slot + 64 * g + 16 * s + 4 * c) : 0u;
-    mma_16816(w0, qa[s].x, qb[s].x, qa[s].y, qb[s].y, i4pair_bf16(nib, 0), i4pair_bf16(nib, 8));
-    mma_16816(x0, qa[s].z, qb[s].z, qa[s].w, qb[s].w, i4pair_bf16(nib, 16), i4pair_bf16(nib, 24));
-    const uint2 m8 = (g == 0) ? lds64(slot + mu_off + 32 * s + 8 * c) : make_uint2(0u, 0u);
-    mma_16816(u0, qa[s].x, qb[s].x, qa[s].y, qb[s].y, i8pair_bf16(m8.x), i8pair_bf16(m8.x >> 16));
-    mma_16816(y0, qa[s].z, qb[s].z, qa[s].w, qb[s].w, i8pair_bf16(m8.y), i8pair_bf16(m8.y >> 16));
+    // elements 32s + 8c .. +7 of basis row g: one word of biased nibbles
+    // (a row past the rank reads as all-zero codes)
+    const uint32_t nib = (g < r) ? lds32(slot + 64 * g + 16 * s + 4 * c) : 0x88888888u;
+    mma_16816(w0, qa[s].x, qb[s].x, qa[s].y, qb[s].y, u4pair_bf16(nib, 0), u4pair_bf16(nib, 4));
+    mma_16816(x0, qa[s].z, qb[s].z, qa[s].w, qb[s].w, u4pair_bf16(nib, 8), u4pair_bf16(nib, 12));
   }
   // column j of W gets s_v[j] * s_c[j] (and the base-2 logit scale)
   const int j0 = 2 * c, j1 = 2 * c + 1;
@@ -263,14 +268,10 @@ __device__ __forceinline__ void compute_page_q4(uint32_t slot, const uint4 (&qa)
   const float f1 = j1 < r ? __uint_as_float(lds32(slot + sc_off + 4 * j1)) *
                                 __uint_as_float(lds32(slot + sc_off + 4 * (r + j1))) * scale_log2
                           : 0.f;
-  const float fmu = __uint_as_float(lds32(slot + sc_off + 8 * r)) * scale_log2;
-  // q . mu of this lane's head rows, held by lane (g, 0)
-  const float qmu0 = __shfl_sync(0xffffffffu, (u0[0] + y0[0]) * fmu, lane & ~3);
-  const float qmu1 = __shfl_sync(0xffffffffu, (u0[2] + y0[2]) * fmu, lane & ~3);
   const float wa = (w0[0] + x0[0]) * f0, wb = (w0[1] + x0[1]) * f1;
   const float wc = (w0[2] + x0[2]) * f0, wd = (w0[3] + x0[3]) * f1;
   auto coef = [&](int jt) -> uint32_t {
-    return (2 * c < r) ? i8pair_bf16(lds16(slot + coef_off + (8 * jt + g) * r + 2 * c)) : 0u;
+    return (2 * c < r) ? u8pair_bf16(lds16(slot + coef_off + (8 * jt + g) * r + 2 * c), 0) : 0u;
   };
 
   if (GRP2) {
@@ -292,7 +293,7 @@ __device__ __forceinline__ void compute_page_q4(uint32_t slot, const uint4 (&qa)
       mma_16816(d[jt], ha0, 0u, ha2, 0u, cbv[2 * jt], cbv[2 * jt + 1]);
     }
     float v[8] = {d[0][0], d[0][1], d[1][0], d[1][1], d[2][0], d[2][1], d[3][0], d[3][1]};
-    e0 = lse2_lanes<8, 1, 2, 16>(v) + qmu0;
+    e0 = lse2_lanes<8, 1, 2, 16>(v);
     e1 = 0.f;
     return;
   }
@@ -317,7 +318,7 @@ __device__ __forceinline__ void compute_page_q4(uint32_t slot, const uint4 (&qa)
     v[2 * jt] = d[jt][0];
     v[2 * jt + 1] = d[jt][1];
   }
-  e0 = lse2_lanes<16, 1, 2, 0>(v) + qmu0;
+  e0 = lse2_lanes<16, 1, 2, 0>(v);
   e1 = 0.f;
   if (G16) {
 #pragma unroll
@@ -325,8 +326,27 @@ __device__ __forceinline__ void compute_page_q4(uint32_t slot, const uint4 (&qa)
       v[2 * jt] = d[jt][2];
       v[2 * jt + 1] = d[jt][3];
     }
-    e1 = lse2_lanes<16, 1, 2, 0>(v) + qmu1;
+    e1 = lse2_lanes<16, 1, 2, 0>(v);
   }
+}
+
+// q . mu for up to kMuBatch staged pages of one warp: one MMA tile whose
+// column n is page n's centroid codes (biased bytes, exact in bf16); lane
+// (g, c) ends with the dot products of head rows g and g + 8 with pages 2c
+// and 2c + 1 (u[0..1] and u[2..3]).
+__device__ __forceinline__ void mu_batch(uint32_t stage_mu, int nb, const uint4 (&qa)[4], const uint4 (&qb)[4],
+                                         int lane, float (&u)[4]) {
+  const int g = lane >> 2, c = lane & 3;
+  float y[4] = {0.f, 0.f, 0.f, 0.f};
+  u[0] = u[1] = u[2] = u[3] = 0.f;
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    const uint2 m8 = (g < nb) ? lds64(stage_mu + 128 * g + 32 * s + 8 * c) : make_uint2(0x80808080u, 0x80808080u);
+    mma_16816(u, qa[s].x, qb[s].x, qa[s].y, qb[s].y, u8pair_bf16(m8.x, 0), u8pair_bf16(m8.x, 2));
+    mma_16816(y, qa[s].z, qb[s].z, qa[s].w, qb[s].w, u8pair_bf16(m8.y, 0), u8pair_bf16(m8.y, 2));
+  }
+#pragma unroll
+  for (int e = 0; e < 4; ++e) u[e] += y[e];
 }
 
 template <bool G16, bool R16, bool GRP2, bool Q4>
@@ -445,6 +465,47 @@ __global__ void __launch_bounds__(kScanThreads, 2) scan_kernel(const ScanArgs a)
       }
     }
     unsigned long long cyc_wait = 0, cyc_comp = 0;
+    // quantised format: this warp's pending pages (centroid codes, centroid
+    // scales and base-2 LSEs per head row), flushed kMuBatch at a time
+    const uint32_t stage_end = ring + RG::kSlots * RG::kSlot;
+    const uint32_t st_mu = stage_end + (uint32_t)(warp * kMuBatch * 128);
+    float* st_smu = reinterpret_cast<float*>(ring_raw + (stage_end - smem_u32(ring_raw)) + kStageMu) + warp * kMuBatch;
+    float* st_pend = reinterpret_cast<float*>(ring_raw + (stage_end - smem_u32(ring_raw)) + kStageMu + kStageSmu) +
+                     warp * kMuBatch * 16;
+    int npend = 0, kdone = 0;
+    uint32_t vmask = 0;
+    auto flush = [&](int nb) {  // warp-uniform
+      __syncwarp();
+      float u[4];
+      mu_batch(st_mu, nb, qa, qb, lane, u);
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int nn = 2 * c + hh;
+        if (nn < nb && ((vmask >> nn) & 1u)) {
+          const float sm = st_smu[nn] * a.scale_log2;
+          const int j = j0 + warp + kScanWarps * (kdone + nn);
+          const float v0 = st_pend[nn * 16 + g] + u[hh] * sm;
+          lse2_merge(zm0, zl0, v0, 1.f);
+          float v1 = 0.f;
+          if (G16) {
+            v1 = st_pend[nn * 16 + g + 8] + u[2 + hh] * sm;
+            lse2_merge(zm1, zl1, v1, 1.f);
+          }
+          float* dst = a.shat + ((size_t)bh * a.max_pages + j) * G;
+          if (g < G && (!GRP2 || g < 4)) dst[g] = v0 * kLn2;
+          if (G16 && g + 8 < G) dst[g + 8] = v1 * kLn2;
+          if (a.page_lse) {
+            float* pl = a.page_lse + ((size_t)b * Hq + (size_t)hkv * G) * a.max_pages + j;
+            if (g < G && (!GRP2 || g < 4)) pl[(size_t)g * a.max_pages] = v0 * kLn2;
+            if (G16 && g + 8 < G) pl[(size_t)(g + 8) * a.max_pages] = v1 * kLn2;
+          }
+        }
+      }
+      __syncwarp();  // the staging area is free again
+      kdone += nb;
+      npend = 0;
+      vmask = 0;
+    };
     for (int p = warp; p < n; p += kScanWarps) {
       const int s = p % S;
       const unsigned long long t0 = trace_clock();
@@ -462,10 +523,26 @@ __global__ void __launch_bounds__(kScanThreads, 2) scan_kernel(const ScanArgs a)
         else
           compute_page<G16, R16, GRP2>(ring + s * RG::kSlot, qa, qb, r, a.scale_log2, lane, e0, e1);
       }
+      if (Q4 && valid) {
+        // stage the centroid codes (one word per lane), its scale and the LSEs
+        const uint32_t slot = ring + s * RG::kSlot;
+        sts32(st_mu + 128 * npend + 4 * lane, lds32(slot + 64 * r + 4 * lane));
+        if (lane == 0) st_smu[npend] = __uint_as_float(lds32(slot + 128 * r + kHeadDim + 8 * r));
+        if (c == 0) {
+          st_pend[npend * 16 + g] = e0;
+          if (G16) st_pend[npend * 16 + g + 8] = e1;
+        }
+      }
       __syncwarp();  // every lane is done with the slot
       if (lane == 0) mbar_arrive(&empty_bar[s]);
       cyc_wait += t1 - t0;
       cyc_comp += trace_clock() - t1;
+      if (Q4) {
+        vmask |= (valid ? 1u : 0u) << npend;
+        if (!valid && lane == 0) set_error(a.err, LOCKS_DEVERR_BLOCK_TABLE);
+        if (++npend == kMuBatch) flush(kMuBatch);
+        continue;
+      }
       if (!valid) {
         if (lane == 0) set_error(a.err, LOCKS_DEVERR_BLOCK_TABLE);
         continue;
@@ -482,6 +559,15 @@ __global__ void __launch_bounds__(kScanThreads, 2) scan_kernel(const ScanArgs a)
           if (g < G && (!GRP2 || g < 4)) pl[(size_t)g * a.max_pages] = e0 * kLn2;
           if (G16 && g + 8 < G) pl[(size_t)(g + 8) * a.max_pages] = e1 * kLn2;
         }
+      }
+    }
+    if (Q4) {
+      if (npend > 0) flush(npend);
+      // each lane of a head row merged different pages
+#pragma unroll
+      for (int o = 1; o <= 2; o <<= 1) {
+        lse2_merge(zm0, zl0, __shfl_xor_sync(0xffffffffu, zm0, o), __shfl_xor_sync(0xffffffffu, zl0, o));
+        if (G16) lse2_merge(zm1, zl1, __shfl_xor_sync(0xffffffffu, zm1, o), __shfl_xor_sync(0xffffffffu, zl1, o));
       }
     }
     if (lane == 0) {
