@@ -85,6 +85,18 @@ def residency(rank: int, page: int = P, d: int = D, basis_bits=16, coef_bits=16,
     return summ / (2 * page * d * 2)
 
 
+def max_over_ranks(value: float, world: int) -> float:
+    """The largest of every rank's value (the job's time is its slowest
+    replica's); the process group must be initialised when world > 1."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def _scan_source_sha() -> str:
     with open(os.path.join(ROOT, "sparse_kv_page_rank_gb300", "csrc", "scan.cu"), "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
@@ -347,11 +359,7 @@ def run_gpu(args):
             s1.record(stream)
         s1.synchronize()
         torch.cuda.synchronize()
-        ms = s0.elapsed_time(s1)
-        if world > 1:
-            t = torch.tensor([ms], dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
+        ms = max_over_ranks(s0.elapsed_time(s1), world)
         del gw, gk
         return ms / K
 
