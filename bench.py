@@ -51,10 +51,13 @@ P, D = 64, 128
 # workloads (profiles/scan_kernel_llama128k.md, profiles/scan_kernel_ctx1m.md);
 # valid only while scan.cu is unchanged since those captures.
 SCAN_TRAFFIC_PER_PAGE_HEAD = {
-    "llama128k": (50372352 + 1536) / 16384,
-    "ctx1m": (100762112 + 3124480) / 32768,
+    "llama128k": (50365952 + 31232) / 16384,
 }
-SCAN_TRAFFIC_SOURCE_SHA = "085ec03a1bf11439"
+# the same for the quantised summary format (profiles/scan_kernel_q4_llama128k.md)
+SCAN_Q4_TRAFFIC_PER_PAGE_HEAD = {
+    "llama128k": (20229632 + 0) / 16384,
+}
+SCAN_TRAFFIC_SOURCE_SHA = "dffae15537cd5e27"
 
 
 # ---------------------------------------------------------------------------
@@ -374,6 +377,14 @@ def run_gpu(args):
         timed(step_fn, K, W)
         timed(dense_fn, K, W)
         timed(scan_fn, K, W)
+        if r <= 8 and not args.no_q4:
+            # the quantised format's step and scan, after the bf16 ones
+            qrts = [LocksRuntime(rt_.k_pool, rt_.v_pool, bt, sl, ns, Hq, r, budget, quantized=True) for rt_ in rts]
+            qrts[0].build_summaries(pages)
+            for qrt in qrts[1:]:
+                qrt.set_summaries(qrts[0].basis_t, None)
+            timed(lambda i, rt_: qrts[i].decode_step(q, stream=stream), K, W)
+            timed(lambda i, rt_: qrts[i].page_scores(q, page_lse_bufs[i], stream=stream), K, W)
         print(json.dumps({"profile": args.config, "copies": R, "steps": K, "warmup": W}))
         return
     clocks = ClockSampler(local)
@@ -467,9 +478,13 @@ def run_gpu(args):
                 qkept += sum(int(cpg) in cs for cpg in case.carriers[b, h] if cpg >= 0)
         qb = q4_page_head_bytes(r)
         q_scan_alg = Hkv * int(nsum_host.sum()) * (qb + G * 4)
+        q_traffic = None
+        if args.config in SCAN_Q4_TRAFFIC_PER_PAGE_HEAD and SCAN_TRAFFIC_SOURCE_SHA == _scan_source_sha():
+            q_traffic = SCAN_Q4_TRAFFIC_PER_PAGE_HEAD[args.config] * Hkv * int(nsum_host.sum())
         q4 = {"value": q4_step_ms * 1e3, "unit": "us", "summary_bytes_per_page_head": qb,
               "residency": qb / (2 * P * D * 2), "speedup_vs_dense": dense_ms / q4_step_ms,
               "scan_us": q4_scan_ms * 1e3, "scan_gbs": q_scan_alg / (q4_scan_ms * 1e-3) / 1e9,
+              "scan_algorithmic_bytes": q_scan_alg, "scan_traffic": q_traffic,
               "mass_recall": float(np.mean(qrec)), "carrier_retention": qkept / total if total else None,
               "summary_build": {"pages_per_s": pages.numel() * Hkv / (q4_build_ms / 1e3), "ms": q4_build_ms},
               "format": "centred; int4 basis, int8 coefficients and centroid, float32 scales per vector"}
