@@ -26,7 +26,11 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - All pointers in the structs and arguments are DEVICE pointers unless
- *    stated otherwise.  The caller owns every buffer and the stream; the
+ *    stated otherwise.  The query, output and lse buffers (q, out, lse) may
+ *    instead be page-locked host memory that the device can address
+ *    (cudaHostAlloc / cudaHostRegister with unified addressing): the kernels
+ *    then read the query and write the results in place over the CPU-GPU
+ *    link, with no separate copy.  The caller owns every buffer and the stream; the
  *    library allocates nothing, frees nothing and never synchronises the
  *    stream (except locks_get_device_error, which reads back one word).
  *  - Element types: keys, values, queries, outputs and summaries are bf16
@@ -125,11 +129,14 @@ typedef struct locks_cache {
  *            rank 2..8.  Then basis_t points to one block of
  *            LOCKS_Q4_PAGE_HEAD_BYTES(rank) bytes per page-head,
  *            [pages_total][num_kv_heads][bytes], and coeffs is unused:
- *              byte 0       basis: row j (j < rank) at 64 j, element t at
- *                           64 j + t/2, low nibble for even t, two's complement
- *                           codes in [-7, 7]
- *              byte 64r     centroid mu: 128 int8 codes in [-127, 127]
- *              byte 64r+128 coefficients: int8 codes [page_size][rank]
+ *              byte 0       basis: row j (j < rank) at 64 j; each 32-bit
+ *                           little-endian word w holds elements 8m .. 8m+7 of
+ *                           the row (m = word index in the row), element 8m+i
+ *                           in bits 4(i/2) + 16(i%2) .. +3, as the code + 8
+ *                           (codes in [-7, 7])
+ *              byte 64r     centroid mu: 128 bytes, code + 128 (codes in
+ *                           [-127, 127])
+ *              byte 64r+128 coefficients: [page_size][rank] bytes, code + 128
  *              byte 128r+128 float32 scales: basis s_v[rank], coefficients
  *                           s_c[rank], centroid s_mu
  *            The summary stands for V_j = s_v[j] * code, c_i[j] = s_c[j] *

@@ -356,3 +356,22 @@ def test_builder_summaries_drive_selection():
                         total += 1
                         kept += int(cpg) in chosen
         assert kept / total >= 0.9, (name, kept, total)
+
+
+def test_decode_step_with_host_query_and_output():
+    """q and out in page-locked host memory (read and written in place by the
+    kernels) give bit-identical results to device buffers."""
+    case = make_case(2, 8, 2, [64 * 30 + 9, 64 * 25 + 63], true_rank=(4, 10), n_carriers=2, seed=71)
+    basis_t, coeffs = oracle_summaries_bf16(case, 8)
+    rt, q = make_runtime(case, 8, 640)
+    _upload_summaries(rt, basis_t, coeffs)
+    out_dev, lse_dev = rt.decode_step(q)
+    out_dev, lse_dev = out_dev.clone(), lse_dev.clone()
+    q_host = q.cpu().pin_memory()
+    out_host = torch.zeros(out_dev.shape, dtype=torch.bfloat16).pin_memory()
+    lse_host = torch.zeros(lse_dev.shape, dtype=torch.float32).pin_memory()
+    rt.decode_step(q_host, out=out_host, lse=lse_host)
+    torch.cuda.synchronize()
+    assert rt.device_error() == 0
+    assert torch.equal(out_host.view(torch.int16), out_dev.cpu().view(torch.int16))
+    assert torch.equal(lse_host, lse_dev.cpu())
