@@ -34,10 +34,13 @@ def pack_q4(qs: dict, r: int) -> np.ndarray:
     """One oracle-quantised page-head summary in the LOCKS_DTYPE_Q4 byte layout."""
     nbytes = (136 * r + 132 + 15) // 16 * 16
     buf = np.zeros(nbytes, dtype=np.uint8)
-    nib = (np.asarray(qs["vq"]) & 15).astype(np.uint8)  # [r][128] two's-complement nibbles
-    buf[:64 * r] = (nib[:, 0::2] | (nib[:, 1::2] << 4)).reshape(-1)
-    buf[64 * r:64 * r + 128] = np.asarray(qs["muq"]).astype(np.int8).view(np.uint8)
-    buf[64 * r + 128:128 * r + 128] = np.asarray(qs["cq"]).astype(np.int8).reshape(-1).view(np.uint8)
+    u = (np.asarray(qs["vq"]) + 8).astype(np.uint32).reshape(r, 16, 8)  # [row][word][element], code + 8
+    words = np.zeros((r, 16), dtype=np.uint32)
+    for i in range(8):
+        words |= u[:, :, i] << np.uint32(4 * (i // 2) + 16 * (i % 2))
+    buf[:64 * r] = words.astype("<u4").view(np.uint8).reshape(-1)
+    buf[64 * r:64 * r + 128] = (np.asarray(qs["muq"]) + 128).astype(np.uint8)
+    buf[64 * r + 128:128 * r + 128] = (np.asarray(qs["cq"]) + 128).astype(np.uint8).reshape(-1)
     scales = np.concatenate([qs["sv"], qs["sc"], [qs["smu"]]]).astype(np.float32)
     buf[128 * r + 128:128 * r + 128 + 4 * (2 * r + 1)] = scales.view(np.uint8)
     return buf
@@ -46,14 +49,13 @@ def pack_q4(qs: dict, r: int) -> np.ndarray:
 def unpack_q4(buf: np.ndarray, r: int, P: int = 64, d: int = 128) -> dict:
     """Inverse of pack_q4 (reads the ABI layout back into codes and scales)."""
     buf = np.asarray(buf, dtype=np.uint8)
-    packed = buf[:64 * r].reshape(r, d // 2)
-    lo = (packed & 15).astype(np.int64)
-    hi = (packed >> 4).astype(np.int64)
-    vq = np.empty((r, d), dtype=np.int64)
-    vq[:, 0::2] = np.where(lo > 7, lo - 16, lo)
-    vq[:, 1::2] = np.where(hi > 7, hi - 16, hi)
-    muq = buf[64 * r:64 * r + 128].view(np.int8).astype(np.int64)
-    cq = buf[64 * r + 128:128 * r + 128].view(np.int8).astype(np.int64).reshape(P, r)
+    words = buf[:64 * r].copy().view("<u4").reshape(r, d // 8).astype(np.int64)
+    vq = np.empty((r, d // 8, 8), dtype=np.int64)
+    for i in range(8):
+        vq[:, :, i] = ((words >> (4 * (i // 2) + 16 * (i % 2))) & 15) - 8
+    vq = vq.reshape(r, d)
+    muq = buf[64 * r:64 * r + 128].astype(np.int64) - 128
+    cq = (buf[64 * r + 128:128 * r + 128].astype(np.int64) - 128).reshape(P, r)
     sc = buf[128 * r + 128:128 * r + 128 + 4 * (2 * r + 1)].view(np.float32).astype(np.float64)
     return dict(vq=vq, sv=sc[:r], cq=cq, sc=sc[r:2 * r], muq=muq, smu=float(sc[2 * r]))
 
