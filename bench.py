@@ -345,9 +345,13 @@ def run_gpu(args):
         torch.cuda.synchronize()
         return g
 
-    def timed(fn, K, W):
+    replay_ms = []
+
+    def timed(fn, K, W, extra_replays=0):
         """Device time per call over exactly K calls (one graph of K calls),
-        after a graph of W warm-up calls."""
+        after a graph of W warm-up calls.  extra_replays further replays of
+        the same graph are timed one by one into replay_ms (for percentiles;
+        the returned value is the first replay's)."""
         gw, gk = capture(fn, W), capture(fn, K)
         with torch.cuda.stream(stream):
             gw.replay()
@@ -363,6 +367,14 @@ def run_gpu(args):
         s1.synchronize()
         torch.cuda.synchronize()
         ms = max_over_ranks(s0.elapsed_time(s1), world)
+        replay_ms.clear()
+        for _ in range(extra_replays):
+            with torch.cuda.stream(stream):
+                s0.record(stream)
+                gk.replay()
+                s1.record(stream)
+            s1.synchronize()
+            replay_ms.append(max_over_ranks(s0.elapsed_time(s1), world) / K)
         del gw, gk
         return ms / K
 
@@ -390,7 +402,8 @@ def run_gpu(args):
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    step_ms = timed(step_fn, K, W)
+    step_ms = timed(step_fn, K, W, extra_replays=9)
+    step_pct = {f"p{p}": float(np.percentile(np.array([step_ms] + replay_ms) * 1e3, p)) for p in (10, 50, 90)}
     clk = clocks.stop()
     dense_ms = timed(dense_fn, max(20, K // 4), W)
     scan_ms = timed(scan_fn, K, W)
@@ -526,7 +539,7 @@ def run_gpu(args):
 
     line = {
         "metric": METRIC, "value": step_us, "unit": "us", "n_gpus": world, "steps": K, "warmup": W,
-        "ms_per_step": step_ms, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "ms_per_step": step_ms, "step_us_over_replays": step_pct, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
         "config": _config_dict(args.config, case, cfg, {
             "l2": f"rotating {R} independent copies of cache + summaries "
@@ -562,6 +575,109 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+def run_growing(args):
+    """The growing-cache loop of the batch-32 8K workload: each decode step
+    appends one token to every sequence (lengths are advanced on the device,
+    inside the graph), and whenever the sequences' last pages fill, the
+    builder summarises them on a side stream while the next 64 steps run; the
+    summarised-page counts advance once the build is done.  Reports the step
+    time with and without the builder running beside it, and the builder's
+    in-loop page-heads per second against the fill rate."""
+    import torch
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    from sparse_kv_page_rank_gb300.build_lib import build
+    build()
+    from sparse_kv_page_rank_gb300.runtime import LocksRuntime
+
+    segments = max(2, args.growing_segments)
+    start = 8192
+    case, cfg = make_config_case("growing", context=start + P * segments)
+    r, budget = cfg["rank"], cfg["budget_tokens"]
+    B, Hq, Hkv = case.batch, case.num_q_heads, case.num_kv_heads
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    k, v = to_dev(case.k_pool), to_dev(case.v_pool)
+    bt = torch.from_numpy(case.block_table).to(dev)
+    q = torch.from_numpy(case.q.view(np.int16)).view(torch.bfloat16).to(dev)
+    runs = {}
+    for overlap in (False, True):
+        sl = torch.full((B,), start, dtype=torch.int32, device=dev)
+        ns = torch.full((B,), start // P, dtype=torch.int32, device=dev)
+        rt = LocksRuntime(k, v, bt, sl, ns, Hq, r, budget)
+        first = torch.from_numpy(np.concatenate([case.block_table[b, :start // P] for b in range(B)])).to(dev)
+        rt.build_summaries(first)
+        main, side = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        one = torch.ones((B,), dtype=torch.int32, device=dev)
+
+        def segment():
+            for _ in range(P):
+                sl.add_(one)
+                rt.decode_step(q, stream=main)
+
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(main):
+            segment()  # warm-up (advances the lengths; reset below)
+            with torch.cuda.graph(g, stream=main):
+                segment()
+        torch.cuda.synchronize()
+        sl.fill_(start)
+        assert rt.device_error() == 0
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        seg_done = [torch.cuda.Event() for _ in range(segments)]
+        built = [torch.cuda.Event() for _ in range(segments)]
+        build_ms = []
+        # the physical pages that fill at the end of each segment
+        fill_ids = [bt[:, start // P + si].contiguous() for si in range(segments)]
+        torch.cuda.synchronize()
+        with torch.cuda.stream(main):
+            e0.record(main)
+            for si in range(segments):
+                if overlap and si >= 2:
+                    # the page filled two segments ago is summarised by now
+                    main.wait_event(built[si - 2])
+                    ns.add_(one)
+                g.replay()
+                seg_done[si].record(main)
+                if overlap and si + 1 < segments:
+                    # the page that just filled: build it beside the next segment
+                    ids = fill_ids[si]
+                    side.wait_event(seg_done[si])
+                    b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    b0.record(side)
+                    rt.build_summaries(ids, stream=side)
+                    b1.record(side)
+                    built[si].record(side)
+                    build_ms.append((b0, b1))
+            e1.record(main)
+        torch.cuda.synchronize()
+        assert rt.device_error() == 0
+        total_ms = e0.elapsed_time(e1)
+        bms = [a.elapsed_time(b) for a, b in build_ms]
+        runs[overlap] = dict(step_us=total_ms * 1e3 / (segments * P), build_ms=bms,
+                             final_n_summarized=int(ns[0].item()), final_seq_len=int(sl[0].item()))
+    ph_per_build = B * Hkv
+    fill_rate = ph_per_build / (runs[True]["step_us"] * P * 1e-6)  # page-heads filled per second
+    mean_build = float(np.mean(runs[True]["build_ms"])) if runs[True]["build_ms"] else None
+    line = {
+        "metric": "growing-cache decode step us with the summary builder beside it",
+        "value": runs[True]["step_us"], "unit": "us", "higher_is_better": False, "n_gpus": 1,
+        "config": _config_dict("growing", case, cfg, {
+            "loop": f"{segments} x 64 steps from {start} tokens; lengths advanced on the device; "
+                    f"one page per sequence fills every 64 steps"}),
+        "step_us_without_builder": runs[False]["step_us"],
+        "builder_overhead_frac": runs[True]["step_us"] / runs[False]["step_us"] - 1.0,
+        "build_ms_per_fill": mean_build,
+        "builder_page_heads_per_s_in_loop": ph_per_build / (mean_build * 1e-3) if mean_build else None,
+        "fill_rate_page_heads_per_s": fill_rate,
+        "final_n_summarized": runs[True]["final_n_summarized"], "final_seq_len": runs[True]["final_seq_len"],
+    }
+    print(json.dumps(line))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -574,8 +690,13 @@ def main():
     ap.add_argument("--copies", type=int, default=0, help="independent cache copies to rotate (0 = auto)")
     ap.add_argument("--profile", action="store_true", help="only replay the step, dense and scan graphs")
     ap.add_argument("--no-q4", action="store_true", help="skip the quantised summary format's measurements")
+    ap.add_argument("--growing-loop", action="store_true",
+                    help="the batch-32 growing-cache loop with the builder on a side stream")
+    ap.add_argument("--growing-segments", type=int, default=6, help="64-step segments in the growing loop")
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.growing_loop:
+        run_growing(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)
