@@ -678,6 +678,77 @@ def run_growing(args):
     print(json.dumps(line))
 
 
+def run_batch_sweep(args):
+    """Batched decode throughput at 256K context (32 query / 8 KV heads, r = 8,
+    budget 2048): tokens per second of the sparse step against the in-library
+    dense decode at several batch sizes.  The caches are drawn on the device
+    (seeded normal keys and values, a random permutation as block table) and
+    summarised by the builder; recall is not measured here, only time."""
+    import torch
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    from sparse_kv_page_rank_gb300.build_lib import build
+    build()
+    from sparse_kv_page_rank_gb300.runtime import LocksRuntime
+
+    ctx, Hq, Hkv, r, budget = 256 * 1024, 32, 8, 8, 2048
+    npg = ctx // P
+    gen = torch.Generator(device=dev)
+    results = []
+    for B in args.batches:
+        gen.manual_seed(1000 + B)
+        pt = B * npg
+        k = torch.empty((pt, Hkv, P, D), dtype=torch.bfloat16, device=dev)
+        v = torch.empty_like(k)
+        for lo in range(0, pt, 4096):
+            hi = min(pt, lo + 4096)
+            k[lo:hi].normal_(generator=gen)
+            v[lo:hi].normal_(generator=gen)
+        bt = torch.randperm(pt, generator=gen, device=dev).to(torch.int32).view(B, npg)
+        sl = torch.full((B,), ctx, dtype=torch.int32, device=dev)
+        ns = torch.full((B,), npg, dtype=torch.int32, device=dev)
+        q = torch.randn((B, Hq, D), generator=gen, device=dev).to(torch.bfloat16)
+        rt = LocksRuntime(k, v, bt, sl, ns, Hq, r, budget)
+        rt.build_summaries(bt.reshape(-1))
+        torch.cuda.synchronize()
+        stream = torch.cuda.Stream(device=dev)
+
+        def per_call(fn, K):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                fn()
+                with torch.cuda.graph(g, stream=stream):
+                    for _ in range(K):
+                        fn()
+            torch.cuda.synchronize()
+            with torch.cuda.stream(stream):
+                g.replay()  # warm-up replay
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+            e1.synchronize()
+            return e0.elapsed_time(e1) / K
+
+        step_ms = per_call(lambda: rt.decode_step(q, stream=stream), 20)
+        dense_ms = per_call(lambda: rt.dense_decode(q, rt.out, rt.lse, stream=stream), 5)
+        assert rt.device_error() == 0
+        results.append({"batch": B, "step_us": step_ms * 1e3, "dense_us": dense_ms * 1e3,
+                        "tokens_per_s": B / (step_ms * 1e-3), "dense_tokens_per_s": B / (dense_ms * 1e-3),
+                        "speedup": dense_ms / step_ms})
+        del rt, k, v, bt, q
+        torch.cuda.empty_cache()
+    print(json.dumps({"metric": "batched decode tokens/s at 256K context (one attention layer), sparse vs dense",
+                      "unit": "tokens/s", "higher_is_better": True, "n_gpus": 1,
+                      "config": {"workload": "256K context, 32 q heads / 8 kv heads, head_dim 128, page 64, rank 8, "
+                                             "budget 2048 tokens, bf16; keys and values drawn on the device",
+                                 "batches": list(args.batches)},
+                      "results": results}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -693,8 +764,12 @@ def main():
     ap.add_argument("--growing-loop", action="store_true",
                     help="the batch-32 growing-cache loop with the builder on a side stream")
     ap.add_argument("--growing-segments", type=int, default=6, help="64-step segments in the growing loop")
+    ap.add_argument("--batch-sweep", action="store_true", help="batched throughput at 256K context")
+    ap.add_argument("--batches", type=int, nargs="+", default=[8, 32, 64])
     args = ap.parse_args()
-    if args.growing_loop:
+    if args.batch_sweep:
+        run_batch_sweep(args)
+    elif args.growing_loop:
         run_growing(args)
     elif args.impl == "reference":
         run_reference(args)
