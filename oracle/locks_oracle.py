@@ -132,7 +132,7 @@ def build_summaries(k_pool: np.ndarray, page_ids, r: int, centered: bool = False
 
 
 # ---------------------------------------------------------------------------
-# Quantised summary ([expl] §2 "Implementatie", Kwantisatie: the basis is
+# Quantised summary ([expl] §2 "Kernmechanisme", Kwantisatie bullet: the basis is
 # stored in int4, the coefficients and the centroid in int8).  The pages give
 # no scale layout; the reading taken here: symmetric scales, one per basis
 # vector, one per coefficient column and one for the centroid, stored as

@@ -23,7 +23,7 @@
 // Output: basis_t [r][d] (rows = basis vectors, descending singular value)
 // and coeffs [P][r], bf16 or fp32.
 //
-// Quantised format (explainer §2 "Implementatie": centred keys, int4 basis,
+// Quantised format (explainer §2 "Kernmechanisme", Kwantisatie: centred keys, int4 basis,
 // int8 coefficients and centroid): the same steps on the centred keys
 // K~ = K - 1 mu^T (mu = mean key of the page).  The Gram matrix of K~ is A
 // with its row and column means removed (A~_ij = A_ij - m_i - m_j + m, m_i

@@ -1,6 +1,6 @@
 """Parity of the quantised, centred summary format (LOCKS_DTYPE_Q4: int4
 basis, int8 coefficients and centroid, as in the explainer's §2
-"Implementatie") with the fp64 oracle (GPU).
+"Kernmechanisme", Kwantisatie) with the fp64 oracle (GPU).
 
 The oracle quantises its own centred SVD summaries; the same codes and
 scales, packed in the ABI layout, go to the GPU, and both sides then compute

@@ -363,7 +363,7 @@ def test_generator_poison_never_read():
 # --- quantised summary ------------------------------------------------------
 
 def test_quantize_roundtrip_within_half_step():
-    """Quantised storage (explainer §2 'Implementatie': int4 basis, int8
+    """Quantised storage (explainer §2 'Kernmechanisme', Kwantisatie: int4 basis, int8
     coefficients and centroid), symmetric per-vector scales: every value is
     recovered to within half a quantisation step, the largest magnitude maps
     to +-qmax, and every code lies in [-qmax, qmax]."""
