@@ -68,12 +68,12 @@ def summary_bytes_per_page_head(rank: int, page: int = P, d: int = D, bytes_per=
     return (rank * d + page * rank) * bytes_per
 
 
-def step_bytes(batch, hkv, G, n_sum, k, tail_tokens, rank) -> dict:
+def step_bytes(batch, hkv, G, n_sum, k, tail_tokens, rank, page: int = P) -> dict:
     """Algorithmic bytes of one decode step: every summary once, s_hat written
     and read once, K+V of the selected pages and the tail once, q and o."""
-    summ = batch * hkv * n_sum * summary_bytes_per_page_head(rank)
+    summ = batch * hkv * n_sum * summary_bytes_per_page_head(rank, page)
     shat = 2 * batch * hkv * n_sum * G * 4
-    sel = batch * hkv * (k * P + tail_tokens) * D * 2 * 2
+    sel = batch * hkv * (k * page + tail_tokens) * D * 2 * 2
     qo = 2 * batch * hkv * G * D * 2
     return dict(summaries=summ, shat=shat, selected_kv=sel, qo=qo, total=summ + shat + sel + qo)
 
@@ -178,6 +178,7 @@ def _oracle_sample(case, cfg, kv_heads, budget_seconds: float, steps: int | None
     from synth.generator import LocksCase
     r = cfg["rank"]
     G = case.group
+    P = case.page_size
     b = 0
     nfull_all = case.n_full_pages(b)
     nfull = nfull_all if max_pages is None else min(nfull_all, max_pages)
@@ -208,7 +209,7 @@ def _oracle_sample(case, cfg, kv_heads, budget_seconds: float, steps: int | None
         sub, basis, coeffs = subs[i % len(subs)]
         t0 = time.perf_counter()
         O.decode_step(sub.q, sub.k_pool, sub.v_pool, sub.block_table, sub.seq_lens, [nfull], basis, coeffs,
-                      1, cfg["budget_tokens"])
+                      1, cfg["budget_tokens"], page_size=P)
         times.append(time.perf_counter() - t0)
         i += 1
         if steps is not None:
@@ -226,7 +227,7 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    case, cfg = make_config_case(args.config)
+    case, cfg = make_config_case(args.config, page_size=args.page_size)
     W, K = args.warmup, args.steps
     # each step: one (sequence, KV head) problem of the workload on a page
     # window sized so that K + W steps take about two minutes, scaled to a full step
@@ -254,10 +255,11 @@ def run_reference(args):
 
 def _config_dict(name, case, cfg, extra=None):
     d = {"workload": f"{name}: batch {case.batch}, {case.num_q_heads} q heads / {case.num_kv_heads} kv heads, "
-                     f"head_dim {D}, page {P}, context {int(case.seq_lens[0])}, rank {cfg['rank']}, "
+                     f"head_dim {D}, page {case.page_size}, context {int(case.seq_lens[0])}, rank {cfg['rank']}, "
                      f"budget {cfg['budget_tokens']} tokens, bf16",
          "batch": case.batch, "num_q_heads": case.num_q_heads, "num_kv_heads": case.num_kv_heads,
-         "context": int(case.seq_lens[0]), "rank": cfg["rank"], "budget_tokens": cfg["budget_tokens"]}
+         "context": int(case.seq_lens[0]), "page_size": case.page_size, "rank": cfg["rank"],
+         "budget_tokens": cfg["budget_tokens"]}
     if extra:
         d.update(extra)
     return d
@@ -284,9 +286,10 @@ def run_gpu(args):
     from sparse_kv_page_rank_gb300 import locks as L
     from sparse_kv_page_rank_gb300.runtime import LocksRuntime
 
-    case, cfg = make_config_case(args.config)
+    case, cfg = make_config_case(args.config, page_size=args.page_size)
     r, budget = cfg["rank"], cfg["budget_tokens"]
     B, Hq, Hkv, G = case.batch, case.num_q_heads, case.num_kv_heads, case.group
+    P = case.page_size
 
     def to_dev(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
@@ -302,7 +305,7 @@ def run_gpu(args):
     per_copy = k0.numel() * 4 + (r * D + P * r) * 2 * case.pages_total * Hkv
     # bytes one step touches (summaries + selected pages); rotate enough copies
     # that consecutive replays of the same copy are > 4x L2 apart
-    touched = Hkv * int(nsum_host.sum()) * summary_bytes_per_page_head(r) + \
+    touched = Hkv * int(nsum_host.sum()) * summary_bytes_per_page_head(r, P) + \
         B * Hkv * min(budget // P, case.max_pages) * P * D * 4
     R = max(2, min(16, math.ceil(4 * 129e6 / max(touched, 1))))
     if args.copies:
@@ -494,10 +497,11 @@ def run_gpu(args):
                 qrec.append(float(np.mean(np.exp(np.logaddexp.reduce(s_star[:, chosen], axis=1) - tot))))
                 cs = set(chosen.tolist())
                 qkept += sum(int(cpg) in cs for cpg in case.carriers[b, h] if cpg >= 0)
-        qb = q4_page_head_bytes(r)
+        qb = q4_page_head_bytes(r, P)
         q_scan_alg = Hkv * int(nsum_host.sum()) * (qb + G * 4)
         q_traffic = None
-        if args.config in SCAN_Q4_TRAFFIC_PER_PAGE_HEAD and SCAN_TRAFFIC_SOURCE_SHA == _scan_source_sha():
+        if args.config in SCAN_Q4_TRAFFIC_PER_PAGE_HEAD and SCAN_TRAFFIC_SOURCE_SHA == _scan_source_sha() \
+                and P == 64:
             q_traffic = SCAN_Q4_TRAFFIC_PER_PAGE_HEAD[args.config] * Hkv * int(nsum_host.sum())
         q4 = {"value": q4_step_ms * 1e3, "unit": "us", "summary_bytes_per_page_head": qb,
               "residency": qb / (2 * P * D * 2), "speedup_vs_dense": dense_ms / q4_step_ms,
@@ -512,25 +516,25 @@ def run_gpu(args):
     sb = dict(summaries=0, shat=0, selected_kv=0, qo=0, total=0)
     for b in range(B):
         bb = step_bytes(1, Hkv, G, int(nsum_host[b]), int(cnt[b].mean()),
-                        int(case.seq_lens[b]) - int(nsum_host[b]) * P, r)
+                        int(case.seq_lens[b]) - int(nsum_host[b]) * P, r, P)
         for key in sb:
             sb[key] += bb[key]
     db = sum(dense_bytes(1, Hkv, G, int(case.seq_lens[b])) for b in range(B))
-    scan_alg = Hkv * n_sum_tot * (summary_bytes_per_page_head(r) + G * 4)
+    scan_alg = Hkv * n_sum_tot * (summary_bytes_per_page_head(r, P) + G * 4)
     peak, peak_kind = _peaks()
     step_us = step_ms * 1e3
     eff_gbs = sb["total"] / (step_ms * 1e-3) / 1e9
     scan_gbs = scan_alg / (scan_ms * 1e-3) / 1e9
     dense_gbs = db / (dense_ms * 1e-3) / 1e9
     traffic = None
-    if args.config in SCAN_TRAFFIC_PER_PAGE_HEAD and SCAN_TRAFFIC_SOURCE_SHA == _scan_source_sha():
+    if args.config in SCAN_TRAFFIC_PER_PAGE_HEAD and SCAN_TRAFFIC_SOURCE_SHA == _scan_source_sha() and P == 64:
         traffic = SCAN_TRAFFIC_PER_PAGE_HEAD[args.config] * Hkv * n_sum_tot
 
     # CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         from synth import make_config_case as mk
-        case2, cfg2 = mk(args.config)
+        case2, cfg2 = mk(args.config, page_size=P)
         us_full, det = _oracle_sample(case2, cfg2, range(min(Hkv, 2)), args.cpu_seconds)
         cpu = {"value": us_full, "unit": "us", "cores": 1, "kind": "oracle",
                "sample": f"fp64 numpy oracle decode step (summaries precomputed) on KV heads 0-"
@@ -549,7 +553,7 @@ def run_gpu(args):
         "step_frac_of_hbm": eff_gbs / peak,
         "dense_us": dense_ms * 1e3, "dense_effective_gbs": dense_gbs, "speedup_vs_dense": dense_ms / step_ms,
         "step_bytes": sb, "dense_bytes": db, "kv_bytes_ratio": db / sb["total"],
-        "residency": residency(r), "mass_recall": float(np.mean(recalls)),
+        "residency": residency(r, P), "mass_recall": float(np.mean(recalls)),
         "exact_lse_selection_recall": float(np.mean(oracle_recalls)),
         "carrier_retention": kept / total if total else None,
         "summary_build": {"pages_per_s": build_pages_per_s, "ms": build_ms, "page_heads": int(pages.numel() * Hkv)},
@@ -761,6 +765,8 @@ def main():
     ap.add_argument("--copies", type=int, default=0, help="independent cache copies to rotate (0 = auto)")
     ap.add_argument("--profile", action="store_true", help="only replay the step, dense and scan graphs")
     ap.add_argument("--no-q4", action="store_true", help="skip the quantised summary format's measurements")
+    ap.add_argument("--page-size", type=int, default=64, choices=[64, 16],
+                    help="tokens per page (16: the page size the explainer quotes its summary size at)")
     ap.add_argument("--growing-loop", action="store_true",
                     help="the batch-32 growing-cache loop with the builder on a side stream")
     ap.add_argument("--growing-segments", type=int, default=6, help="64-step segments in the growing loop")

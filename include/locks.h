@@ -35,9 +35,10 @@
  *    stream (except locks_get_device_error, which reads back one word).
  *  - Element types: keys, values, queries, outputs and summaries are bf16
  *    (raw 16-bit patterns), lengths and indices int32, scores float32.
- *  - Fixed sizes in this build: head_dim d = 128, page_size P = 64,
- *    group size G = num_q_heads / num_kv_heads in 1..16, summary rank r even
- *    in 2..16.  Other values return LOCKS_ERR_UNSUPPORTED.
+ *  - Sizes in this build: head_dim d = 128, page_size P = 64 or 16 (the
+ *    explainer's §2 "Kernmechanisme" gives a page size of 16), group size
+ *    G = num_q_heads / num_kv_heads in 1..16, summary rank r even in 2..16
+ *    (and r <= P).  Other values return LOCKS_ERR_UNSUPPORTED.
  *  - Query head hq belongs to KV head hq / G (standard GQA grouping).
  *  - Lengths (seq_lens, n_summarized) are read on the device, so a call can be
  *    captured once in a CUDA graph and replayed while the cache grows; all
@@ -87,14 +88,16 @@ typedef enum {
 #define LOCKS_DTYPE_F32 1
 #define LOCKS_DTYPE_Q4 2
 
-/* Bytes of one page-head of a LOCKS_DTYPE_Q4 summary at rank r (head_dim 128,
- * page_size 64): 64r basis + 128 centroid + 64r coefficients + 4(2r+1) scales,
- * rounded up to 16. */
-#define LOCKS_Q4_PAGE_HEAD_BYTES(r) ((((136 * (r)) + 132) + 15) / 16 * 16)
+/* Bytes of one page-head of a LOCKS_DTYPE_Q4 summary at rank r and page size
+ * P (head_dim 128): 64r basis + 128 centroid + P r coefficients + 4(2r+1)
+ * scales, rounded up to 16.  LOCKS_Q4_PAGE_HEAD_BYTES is the P = 64 case. */
+#define LOCKS_Q4_BLOCK_BYTES(r, P) ((((72 * (r)) + ((P) * (r)) + 132) + 15) / 16 * 16)
+#define LOCKS_Q4_PAGE_HEAD_BYTES(r) LOCKS_Q4_BLOCK_BYTES(r, 64)
 
 /* Paged KV cache.  K and V pools hold whole pages for all KV heads:
  *   k_pool, v_pool  bf16 [pages_total][num_kv_heads][page_size][head_dim]
- *                   (one page-head = P x d contiguous, 16 KiB at P=64, d=128;
+ *                   (one page-head = P x d contiguous, 16 KiB at P=64, d=128,
+ *                   4 KiB at P=16;
  *                   base 16-byte aligned)
  *   block_table     int32 [batch][max_pages]: physical page of logical page j
  *                   of sequence b; entries past the sequence are not read
@@ -125,9 +128,9 @@ typedef struct locks_cache {
  *            LOCKS_DTYPE_F32 is accepted by locks_build_summaries only (a
  *            full-precision copy for validation);
  *            LOCKS_DTYPE_Q4: the quantised, centred format of the explainer's
- *            §2 "Implementatie" (int4 basis, int8 coefficients and centroid),
+ *            §2 "Kernmechanisme", Kwantisatie (int4 basis, int8 coefficients and centroid),
  *            rank 2..8.  Then basis_t points to one block of
- *            LOCKS_Q4_PAGE_HEAD_BYTES(rank) bytes per page-head,
+ *            LOCKS_Q4_BLOCK_BYTES(rank, page_size) bytes per page-head,
  *            [pages_total][num_kv_heads][bytes], and coeffs is unused:
  *              byte 0       basis: row j (j < rank) at 64 j; each 32-bit
  *                           little-endian word w holds elements 8m .. 8m+7 of
@@ -137,7 +140,7 @@ typedef struct locks_cache {
  *              byte 64r     centroid mu: 128 bytes, code + 128 (codes in
  *                           [-127, 127])
  *              byte 64r+128 coefficients: [page_size][rank] bytes, code + 128
- *              byte 128r+128 float32 scales: basis s_v[rank], coefficients
+ *              byte 64r+128+P r  float32 scales: basis s_v[rank], coefficients
  *                           s_c[rank], centroid s_mu
  *            The summary stands for V_j = s_v[j] * code, c_i[j] = s_c[j] *
  *            code, mu = s_mu * code, and the page's keys are approximated

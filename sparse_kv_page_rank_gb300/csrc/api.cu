@@ -45,15 +45,16 @@ locks_status_t check_cache(const locks_cache_t* c, bool need_kv) {
   if (!c) return LOCKS_ERR_INVALID_ARG;
   if (c->batch <= 0 || c->num_kv_heads <= 0 || c->pages_total <= 0 || c->max_pages <= 0)
     return LOCKS_ERR_INVALID_ARG;
-  if (c->head_dim != kHeadDim || c->page_size != kPage) return LOCKS_ERR_UNSUPPORTED;
+  if (c->head_dim != kHeadDim || (c->page_size != kPage && c->page_size != 16)) return LOCKS_ERR_UNSUPPORTED;
   if (need_kv) {
     if (!c->k_pool || !c->v_pool || !c->block_table || !c->seq_lens) return LOCKS_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(c->k_pool) | reinterpret_cast<uintptr_t>(c->v_pool)) & 15)
       return LOCKS_ERR_INVALID_ARG;
   }
   // TMA row coordinate and 32-bit page-head offsets
-  if ((long long)c->pages_total * c->num_kv_heads * kPage > 0x7fffffffLL) return LOCKS_ERR_UNSUPPORTED;  // >= basis rows
-  if ((long long)c->max_pages * kPage > 0x7fffffffLL) return LOCKS_ERR_UNSUPPORTED;
+  // (key rows >= basis rows, since r <= 16 <= P)
+  if ((long long)c->pages_total * c->num_kv_heads * c->page_size > 0x7fffffffLL) return LOCKS_ERR_UNSUPPORTED;
+  if ((long long)c->max_pages * c->page_size > 0x7fffffffLL) return LOCKS_ERR_UNSUPPORTED;
   return LOCKS_OK;
 }
 
@@ -90,8 +91,12 @@ Plan make_plan(const locks_cache_t* c, const locks_params_t* p) {
   pl.G = p->num_q_heads / c->num_kv_heads;
   pl.Hq = p->num_q_heads;
   pl.BH = c->batch * c->num_kv_heads;
-  pl.k_max = std::min(p->budget_tokens / kPage, c->max_pages);
+  const int P = c->page_size;
+  pl.k_max = std::min(p->budget_tokens / P, c->max_pages);
   const long long BH = pl.BH;
+  // attention works in 64-token tiles: one page, or four 16-token pages
+  const int ppt = kPage / P;
+  const long long max_tiles = (c->max_pages + ppt - 1) / ppt;
 
   // scan: about two resident CTAs per SM, pages per CTA a multiple of the warp count
   {
@@ -118,22 +123,22 @@ Plan make_plan(const locks_cache_t* c, const locks_params_t* p) {
   // CTAs per SM
   {
     const long long target = 3LL * sms;
-    const int cs_sparse = attend_max_cluster(kAttendSparse);
-    const int cs_dense = attend_max_cluster(kAttendDense);
-    const long long items = (long long)pl.k_max + 2;
+    const int cs_sparse = attend_max_cluster(kAttendSparse, P);
+    const int cs_dense = attend_max_cluster(kAttendDense, P);
+    const long long items = ((long long)pl.k_max + 2 + ppt - 1) / ppt;  // tiles
     // the largest cluster (up to one CTA per item) with which every
     // problem's cluster is resident at once: one wave, no CTA waits for a slot
     int cs = 1;
     while (cs * 2 <= cs_sparse && cs * 2 <= items) cs *= 2;
-    while (cs > 1 && BH > attend_active_clusters(kAttendSparse, cs)) cs /= 2;
+    while (cs > 1 && BH > attend_active_clusters(kAttendSparse, cs, P)) cs /= 2;
     pl.sparse_cluster = cs;
     // dense: the (cluster, clusters-per-problem) shape with the most CTAs
     // that still fits in one wave of `target` resident CTAs
     long long best = -1;
     for (int csd = cs_dense; csd >= 1; csd /= 2) {
-      if (csd > c->max_pages) continue;
+      if (csd > max_tiles) continue;
       long long nc = target / (BH * csd);
-      nc = std::max<long long>(1, std::min<long long>(nc, (c->max_pages + csd - 1) / csd));
+      nc = std::max<long long>(1, std::min<long long>(nc, (max_tiles + csd - 1) / csd));
       const long long ctas = BH * csd * nc;
       // the fullest wave wins; among equals the larger cluster (cheaper
       // on-chip merge), since the loop runs from large to small clusters
@@ -148,7 +153,7 @@ Plan make_plan(const locks_cache_t* c, const locks_params_t* p) {
       pl.dense_nc = 1;
     }
     long long ls = (target + BH - 1) / BH;
-    pl.lse_splits = (int)std::max<long long>(1, std::min<long long>(ls, c->max_pages));
+    pl.lse_splits = (int)std::max<long long>(1, std::min<long long>(ls, max_tiles));
   }
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -210,9 +215,10 @@ bool encode_rows(CUtensorMap* m, const void* pool, const locks_cache_t* c, int r
   return r == CUDA_SUCCESS;
 }
 
-// K or V pool: 64 x 64 boxes (one page-head is two boxes).
+// K or V pool: boxes of one page-head's rows x 64 columns (one page-head is
+// two boxes).
 bool encode_pool(CUtensorMap* m, const void* pool, const locks_cache_t* c) {
-  return encode_rows(m, pool, c, kPage, 64);
+  return encode_rows(m, pool, c, c->page_size, c->page_size);
 }
 
 locks_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? LOCKS_OK : LOCKS_ERR_CUDA; }
@@ -241,6 +247,7 @@ locks_status_t run_select(const locks_cache_t* c, const locks_summary_t* s, cons
   sa.n_chunks = pl.n_scan;
   sa.scale_log2 = scale_of(p) * kLog2e;
   sa.q4 = s->dtype == LOCKS_DTYPE_Q4 ? 1 : 0;
+  sa.page_size = c->page_size;
   cudaError_t e = launch_scan(sa, st, true);
   if (e != cudaSuccess) return LOCKS_ERR_CUDA;
   if (!sel) return LOCKS_OK;  // scan only
@@ -265,6 +272,7 @@ locks_status_t run_select(const locks_cache_t* c, const locks_summary_t* s, cons
   ta.chunk_pages = pl.tk_chunk;
   ta.n_chunks = pl.n_tk;
   ta.smem_keys = pl.tk_keys;
+  ta.page_size = c->page_size;
   return cuda_status(launch_topk(ta, st, true));
 }
 
@@ -308,6 +316,7 @@ locks_status_t run_attend(const locks_cache_t* c, const locks_params_t* p, const
   }
   a.scale_log2 = scale_of(p) * kLog2e;
   a.inputs_early = inputs_early ? 1 : 0;
+  a.page_size = c->page_size;
   return cuda_status(launch_attend(a, tk, tv, mode, st, true));
 }
 
@@ -367,6 +376,7 @@ locks_status_t locks_build_summaries(const locks_cache_t* cache, locks_summary_t
   a.pages_total = cache->pages_total;
   a.format = summary->dtype;
   a.err = ws ? static_cast<int*>(ws) : nullptr;  // the error word is at offset 0 of every workspace
+  a.page_size = cache->page_size;
   return cuda_status(launch_build(a, static_cast<cudaStream_t>(stream)));
 }
 

@@ -26,6 +26,11 @@
 // write their partial to the workspace and the last cluster to finish (atomic
 // ticket, no waiting) merges them, again one column slice per CTA.  The
 // result is o (bf16) and lse (natural log).
+//
+// 16-token pages (the explainer's §2 "Kernmechanisme" page size): a tile is
+// four pages, loaded as four 16-row boxes into the rows 16w..16w+15 that warp
+// w already owns, so the inner loop is the 64-token one and each warp masks
+// by its own page's length.  The CTA ranges are cut on tile boundaries.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -58,7 +63,7 @@ struct Item {
   int len;    // valid tokens in the page (0 when invalid)
 };
 
-template <int MODE>
+template <int MODE, int P>
 __device__ __forceinline__ Item get_item(const AttendArgs& a, int i, int b, int bh, int L, int ns,
                                          int cnt) {
   Item it;
@@ -86,17 +91,21 @@ __device__ __forceinline__ Item get_item(const AttendArgs& a, int i, int b, int 
       it.lp = -1;
     } else {
       it.phys = phys;
-      int rem = L - lp * kPage;
-      it.len = rem < kPage ? rem : kPage;
+      int rem = L - lp * P;
+      it.len = rem < P ? rem : P;
     }
   }
   return it;
 }
 
-template <int MODE, int STAGES>
+template <int MODE, int STAGES, int P>
 __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_constant__ CUtensorMap tk,
                                                                 const __grid_constant__ CUtensorMap tv,
                                                                 const AttendArgs a) {
+  constexpr int kPPT = kPage / P;                  // pages per 64-token tile: 1 or 4
+  constexpr int kTilesPerBatch = kAttendThreads / kPPT;  // tiles whose pages one resolve() covers
+  static_assert(kPPT == 1 || kPPT == kWarps, "one page per warp at P = 16");
+  static_assert(STAGES <= kTilesPerBatch, "the tiles in flight span at most two resolved batches");
   extern __shared__ uint8_t dyn_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_raw) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t bars[STAGES];
@@ -162,14 +171,14 @@ __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_con
   if (a.inputs_early) pdl_wait();
   if (MODE == kAttendSparse) trace_mark(a.err, kTrAttWait, true);
 
-  if (L < 0 || L > a.max_pages * kPage) {
+  if (L < 0 || L > a.max_pages * P) {
     if (tid == 0 && split == 0) set_error(a.err, LOCKS_DEVERR_LENGTHS);
-    L = L < 0 ? 0 : a.max_pages * kPage;
+    L = L < 0 ? 0 : a.max_pages * P;
   }
-  const int n_pages = (L + kPage - 1) / kPage;
+  const int n_pages = (L + P - 1) / P;
   int ns = 0, cnt = 0, n_items;
   if (MODE == kAttendSparse) {
-    const int cap = min(L / kPage, a.max_pages);
+    const int cap = min(L / P, a.max_pages);
     ns = ns_raw < 0 ? 0 : (ns_raw > cap ? cap : ns_raw);
     cnt = a.sel_count[bh];
     const int kcap = min(a.k_max, ns);
@@ -181,18 +190,21 @@ __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_con
   } else {
     n_items = n_pages;
   }
-  const int ipc = (n_items + a.n_splits - 1) / a.n_splits;
+  // pages per CTA: a whole number of tiles
+  const int ipc = ((n_items + a.n_splits - 1) / a.n_splits + kPPT - 1) / kPPT * kPPT;
   const int i0 = min(n_items, split * ipc), i1 = min(n_items, i0 + ipc);
+  const int ntile = (i1 - i0 + kPPT - 1) / kPPT;
 
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t tx_bytes = (MODE == kAttendPageLse) ? kTile : kStage;
+  // bytes one page brings into a stage (K, and V unless page-LSE mode)
+  constexpr uint32_t kPageTx = (uint32_t)P * kHeadDim * 2 * (MODE == kAttendPageLse ? 1 : 2);
   // resolve items [base, base + kAttendThreads) of this CTA: selection entry
   // and block-table entry, all threads at once
   auto resolve = [&](int base) {
     const int i = i0 + base + tid;
     const int buf = (base / kAttendThreads) & 1;
     if (i < i1) {
-      const Item it = get_item<MODE>(a, i, b, bh, L, ns, cnt);
+      const Item it = get_item<MODE, P>(a, i, b, bh, L, ns, cnt);
       it_phys[buf][tid] = it.phys;
       it_len[buf][tid] = it.len;
       it_lp[buf][tid] = it.lp;
@@ -201,21 +213,27 @@ __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_con
   resolve(0);
   __syncthreads();
   if (MODE == kAttendSparse) trace_mark(a.err, kTrAttResolved, false);
-  // thread 0 only; item (i - i0) must lie in the resolved batch
-  auto issue = [&](int stage, int i) {
-    const int k = i - i0;
-    const int y = (it_phys[(k / kAttendThreads) & 1][k % kAttendThreads] * a.num_kv_heads + hkv) * kPage;
+  // thread 0 only; the pages of tile t must lie in the resolved batch.
+  // Page w of a tile lands in rows 16w.. of each 64-row half-tile (byte
+  // offset 2048 w, a multiple of the 1024-byte swizzle period).
+  auto issue = [&](int stage, int t) {
+    const int np = min(kPPT, i1 - i0 - t * kPPT);
     uint8_t* dst = smem + stage * kStage;
-    mbar_arrive_expect_tx(&bars[stage], tx_bytes);
-    tma_load_2d(dst, &tk, &bars[stage], 0, y);
-    tma_load_2d(dst + kHalfTile, &tk, &bars[stage], 64, y);
-    if (MODE != kAttendPageLse) {
-      tma_load_2d(dst + kTile, &tv, &bars[stage], 0, y);
-      tma_load_2d(dst + kTile + kHalfTile, &tv, &bars[stage], 64, y);
+    mbar_arrive_expect_tx(&bars[stage], kPageTx * (uint32_t)np);
+    for (int w = 0; w < np; ++w) {
+      const int k = t * kPPT + w;
+      const int y = (it_phys[(k / kAttendThreads) & 1][k % kAttendThreads] * a.num_kv_heads + hkv) * P;
+      uint8_t* d = dst + w * (P * 128);
+      tma_load_2d(d, &tk, &bars[stage], 0, y);
+      tma_load_2d(d + kHalfTile, &tk, &bars[stage], 64, y);
+      if (MODE != kAttendPageLse) {
+        tma_load_2d(d + kTile, &tv, &bars[stage], 0, y);
+        tma_load_2d(d + kTile + kHalfTile, &tv, &bars[stage], 64, y);
+      }
     }
   };
   if (tid == 0) {
-    for (int s = 0; s < STAGES && i0 + s < i1 && s < kAttendThreads; ++s) issue(s, i0 + s);
+    for (int s = 0; s < STAGES && s < ntile; ++s) issue(s, s);
   }
 
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
@@ -225,11 +243,14 @@ __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_con
 #pragma unroll
   for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 
-  for (int it = 0; i0 + it < i1; ++it) {
+  for (int it = 0; it < ntile; ++it) {
     const int stage = it % STAGES;
     const uint32_t parity = (it / STAGES) & 1;
-    const int item_len = it_len[(it / kAttendThreads) & 1][it % kAttendThreads];
-    const int item_lp = it_lp[(it / kAttendThreads) & 1][it % kAttendThreads];
+    // this warp's page (the tile's only page at P = 64)
+    const int wk = it * kPPT + (kPPT > 1 ? warp : 0);
+    const bool w_in = wk < i1 - i0;
+    const int item_len = w_in ? it_len[(wk / kAttendThreads) & 1][wk % kAttendThreads] : 0;
+    const int item_lp = kPPT > 1 ? 0 : it_lp[(wk / kAttendThreads) & 1][wk % kAttendThreads];
     const bool ok = mbar_wait(&bars[stage], parity);
     if (__syncthreads_or(!ok)) {
       if (tid == 0) set_error(a.err, kDevErrTimeout);
@@ -254,7 +275,8 @@ __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_con
         mma_16816(s[1], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b2, b3);
       }
     }
-    const int len = item_len;
+    // valid rows of the tile for this warp: tokens 16w .. 16w + len of its page
+    const int len = kPPT > 1 ? 16 * warp + item_len : item_len;
     float tm0 = -INFINITY, tm1 = -INFINITY;
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
@@ -343,27 +365,38 @@ __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_con
     fence_proxy_async();
     __syncthreads();
     if (MODE == kAttendPageLse) {
-      if (tid < G && item_lp >= 0) {
-        float mm = -INFINITY, ll = 0.f;
+      if (kPPT == 1) {
+        if (tid < G && item_lp >= 0) {
+          float mm = -INFINITY, ll = 0.f;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) lse2_merge(mm, ll, sm_pl[stage][w][tid].x, sm_pl[stage][w][tid].y);
-        a.page_lse[((size_t)b * Hq + (size_t)hkv * G + tid) * a.max_pages + item_lp] =
-            (mm == -INFINITY) ? -INFINITY : (mm + fast_log2(ll)) * kLn2;
+          for (int w = 0; w < kWarps; ++w) lse2_merge(mm, ll, sm_pl[stage][w][tid].x, sm_pl[stage][w][tid].y);
+          a.page_lse[((size_t)b * Hq + (size_t)hkv * G + tid) * a.max_pages + item_lp] =
+              (mm == -INFINITY) ? -INFINITY : (mm + fast_log2(ll)) * kLn2;
+        }
+      } else if (tid < kWarps * G) {
+        // one page per warp: its own (max, sum) is the page's
+        const int w = tid / G, h = tid % G, k = it * kPPT + w;
+        const int lp = k < i1 - i0 ? it_lp[(k / kAttendThreads) & 1][k % kAttendThreads] : -1;
+        if (lp >= 0) {
+          const float2 ml = sm_pl[stage][w][h];
+          a.page_lse[((size_t)b * Hq + (size_t)hkv * G + h) * a.max_pages + lp] =
+              (ml.x == -INFINITY) ? -INFINITY : (ml.x + fast_log2(ml.y)) * kLn2;
+        }
       }
     }
     // next batch of item descriptors once the current one has been issued
     const int nxt = it + STAGES;
-    if (nxt % kAttendThreads == 0 && i0 + nxt < i1) {
-      resolve(nxt);
+    if (nxt % kTilesPerBatch == 0 && nxt < ntile) {
+      resolve(nxt * kPPT);
       __syncthreads();
     }
-    if (tid == 0 && i0 + nxt < i1) issue(stage, i0 + nxt);
+    if (tid == 0 && nxt < ntile) issue(stage, nxt);
   }
 
   if (failed) {
     // give copies still in flight a bounded time to land before the ring is reused
     if (tid == 0) {
-      for (int it = consumed; it < consumed + STAGES && i0 + it < i1; ++it)
+      for (int it = consumed; it < consumed + STAGES && it < ntile; ++it)
         (void)mbar_wait(&bars[it % STAGES], (it / STAGES) & 1);
     }
     __syncthreads();
@@ -565,11 +598,11 @@ size_t smem_bytes() {
   return (size_t)STAGES * kStage + 1024 + (MODE == kAttendSparse ? kRecvBytes : 0);
 }
 
-template <int MODE, int STAGES>
+template <int MODE, int STAGES, int P>
 cudaError_t launch_mode(const AttendArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t s,
                         bool pdl) {
   const size_t smem = smem_bytes<MODE, STAGES>();
-  auto kern = attend_kernel<MODE, STAGES>;
+  auto kern = attend_kernel<MODE, STAGES, P>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   if (a.cluster > 8) {
@@ -600,9 +633,9 @@ cudaError_t launch_mode(const AttendArgs& a, const CUtensorMap& tk, const CUtens
 
 // How many clusters of cs CTAs of this kernel the device can hold at once
 // (0 when it cannot place one).
-template <int MODE, int STAGES>
+template <int MODE, int STAGES, int P>
 int active_clusters_of(int cs) {
-  auto kern = attend_kernel<MODE, STAGES>;
+  auto kern = attend_kernel<MODE, STAGES, P>;
   const size_t smem = smem_bytes<MODE, STAGES>();
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
   if (cs > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
@@ -627,9 +660,9 @@ int active_clusters_of(int cs) {
 }
 
 // Largest cluster size (16, 8, ... 1) the device can place for this kernel.
-template <int MODE, int STAGES>
+template <int MODE, int STAGES, int P>
 int max_cluster_of() {
-  auto kern = attend_kernel<MODE, STAGES>;
+  auto kern = attend_kernel<MODE, STAGES, P>;
   const size_t smem = smem_bytes<MODE, STAGES>();
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 1;
   for (int cs = 16; cs > 1; cs /= 2) {
@@ -658,38 +691,56 @@ constexpr int kDenseStages = 2;
 
 }  // namespace
 
-int attend_active_clusters(int mode, int cs) {
-  static int cache[2][5][64] = {};
+int attend_active_clusters(int mode, int cs, int page_size) {
+  static int cache[2][2][5][64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || cs < 1 || cs > 16) return 1;
-  const int m = mode == kAttendSparse ? 0 : 1;
+  const int m = mode == kAttendSparse ? 0 : 1, p16 = page_size == 16 ? 1 : 0;
   const int li = 31 - __builtin_clz((unsigned)cs);
-  if (cache[m][li][dev] == 0) {
-    int n = mode == kAttendSparse ? active_clusters_of<kAttendSparse, kSparseStages>(cs)
-                                  : active_clusters_of<kAttendDense, kDenseStages>(cs);
-    cache[m][li][dev] = n > 0 ? n : -1;
+  int& slot = cache[p16][m][li][dev];
+  if (slot == 0) {
+    int n;
+    if (p16)
+      n = mode == kAttendSparse ? active_clusters_of<kAttendSparse, kSparseStages, 16>(cs)
+                                : active_clusters_of<kAttendDense, kDenseStages, 16>(cs);
+    else
+      n = mode == kAttendSparse ? active_clusters_of<kAttendSparse, kSparseStages, kPage>(cs)
+                                : active_clusters_of<kAttendDense, kDenseStages, kPage>(cs);
+    slot = n > 0 ? n : -1;
   }
-  return cache[m][li][dev] > 0 ? cache[m][li][dev] : 0;
+  return slot > 0 ? slot : 0;
 }
 
-int attend_max_cluster(int mode) {
-  static int cache[2][64] = {};
+int attend_max_cluster(int mode, int page_size) {
+  static int cache[2][2][64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 8;
-  const int m = mode == kAttendSparse ? 0 : 1;
-  if (cache[m][dev] == 0)
-    cache[m][dev] = mode == kAttendSparse ? max_cluster_of<kAttendSparse, kSparseStages>()
-                                          : max_cluster_of<kAttendDense, kDenseStages>();
-  return cache[m][dev];
+  const int m = mode == kAttendSparse ? 0 : 1, p16 = page_size == 16 ? 1 : 0;
+  int& slot = cache[p16][m][dev];
+  if (slot == 0) {
+    if (p16)
+      slot = mode == kAttendSparse ? max_cluster_of<kAttendSparse, kSparseStages, 16>()
+                                   : max_cluster_of<kAttendDense, kDenseStages, 16>();
+    else
+      slot = mode == kAttendSparse ? max_cluster_of<kAttendSparse, kSparseStages, kPage>()
+                                   : max_cluster_of<kAttendDense, kDenseStages, kPage>();
+  }
+  return slot;
+}
+
+template <int P>
+cudaError_t launch_page(const AttendArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, int mode,
+                        cudaStream_t s, bool pdl) {
+  switch (mode) {
+    case kAttendSparse: return launch_mode<kAttendSparse, kSparseStages, P>(a, tk, tv, s, pdl);
+    case kAttendDense: return launch_mode<kAttendDense, kDenseStages, P>(a, tk, tv, s, pdl);
+    default: return launch_mode<kAttendPageLse, kDenseStages, P>(a, tk, tv, s, pdl);
+  }
 }
 
 cudaError_t launch_attend(const AttendArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, int mode,
                           cudaStream_t s, bool pdl) {
-  switch (mode) {
-    case kAttendSparse: return launch_mode<kAttendSparse, kSparseStages>(a, tk, tv, s, pdl);
-    case kAttendDense: return launch_mode<kAttendDense, kDenseStages>(a, tk, tv, s, pdl);
-    default: return launch_mode<kAttendPageLse, kDenseStages>(a, tk, tv, s, pdl);
-  }
+  return a.page_size == 16 ? launch_page<16>(a, tk, tv, mode, s, pdl) : launch_page<kPage>(a, tk, tv, mode, s, pdl);
 }
 
 }  // namespace locks

@@ -6,11 +6,14 @@
 // the page keeps its coefficients.  §2 "Implementatie": this happens off the
 // critical path of decoding.
 //
-// For one page-head K (P x d = 64 x 128, bf16) the top-r left singular
-// vectors are the top-r eigenvectors of the Gram matrix A = K K^T (64 x 64).
-// Only r <= 16 of 64 eigenpairs are needed, so one CTA per page-head runs
-//   1. A = K K^T on tensor cores (m16n8k16, bf16 products exact in fp32);
-//   2. subspace iteration with l = r + 8 vectors: X_0 from A times a fixed
+// For one page-head K (P x d = 64 x 128 or 16 x 128, bf16) the top-r left
+// singular vectors are the top-r eigenvectors of the Gram matrix A = K K^T
+// (P x P).  Only r <= 16 of P eigenpairs are needed, so one CTA per page-head
+// runs
+//   1. A = K K^T on tensor cores (m16n8k16, bf16 products exact in fp32;
+//      plain fp32 FMAs for the 16 x 16 product of a 16-token page);
+//   2. subspace iteration with l = min(r + 8, P) vectors (at P = 16 the
+//      whole space, so Rayleigh-Ritz below is exact): X_0 from A times a fixed
 //      +-1 pattern, then X <- orth(A X) for a fixed number of steps
 //      (modified Gram-Schmidt; deterministic, no early exit);
 //   3. Rayleigh-Ritz: T = X^T A X (l x l), eigenpairs of T by a parallel
@@ -31,7 +34,7 @@
 // V = K~^T U_r = K^T U_r - mu (1^T U_r) and C = K~ V = K V - 1 (mu^T V).
 // Each basis vector, coefficient column and the centroid then get one
 // symmetric float32 scale s = max|x| / qmax (qmax 7 for int4, 127 for int8)
-// and codes rint(x / s), packed as LOCKS_Q4_PAGE_HEAD_BYTES(r) bytes.
+// and codes rint(x / s), packed as LOCKS_Q4_BLOCK_BYTES(r, P) bytes.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -42,18 +45,20 @@ namespace {
 constexpr int kBT = 256;            // threads
 constexpr int kBW = kBT / 32;       // warps
 constexpr int kKS = 136;            // bf16 row stride of K in shared memory (conflict-free ldmatrix)
-constexpr int kAS = 65;             // fp32 row stride of A
+template <int P>
+constexpr int kAS = P + 1;          // fp32 row stride of A
 constexpr int kLmax = 24;           // subspace size limit (r <= 16 -> l <= 24)
 constexpr int kXS = kLmax + 1;
 constexpr int kVS = kHeadDim + 1;
 constexpr int kPowerIters = 8;
 constexpr int kJacobiSweeps = 10;
 
+template <int P>
 struct BuildSmem {
-  uint16_t K[kPage * kKS];
-  float A[kPage * kAS];
-  float X[kPage * kXS];
-  float Y[kPage * kXS];
+  uint16_t K[P * kKS];
+  float A[P * kAS<P>];
+  float X[P * kXS];
+  float Y[P * kXS];
   float T[kLmax * kXS];
   float Z[kLmax * kXS];
   float V[16 * kVS];        // basis rows
@@ -63,19 +68,20 @@ struct BuildSmem {
   float red[kBW];
   // quantised format only
   float mu[kHeadDim];  // mean key
-  float rm[kPage];     // row means of A
+  float rm[P];     // row means of A
   float cs[16];        // column sums of U_r, then mu . V_j
   float sv[16], sc[16], smu;
   float grand;
 };
 
-// Y = A X  (64 x l); A symmetric 64 x 64
-__device__ void mul_A(const BuildSmem& s, const float* X, float* Y, int l) {
-  for (int e = threadIdx.x; e < kPage * l; e += kBT) {
+// Y = A X  (P x l); A symmetric P x P
+template <int P>
+__device__ void mul_A(const BuildSmem<P>& s, const float* X, float* Y, int l) {
+  for (int e = threadIdx.x; e < P * l; e += kBT) {
     const int i = e / l, j = e % l;
     float acc = 0.f;
 #pragma unroll 8
-    for (int k = 0; k < kPage; ++k) acc = fmaf(s.A[i * kAS + k], X[k * kXS + j], acc);
+    for (int k = 0; k < P; ++k) acc = fmaf(s.A[i * kAS<P> + k], X[k * kXS + j], acc);
     Y[i * kXS + j] = acc;
   }
 }
@@ -103,15 +109,16 @@ __device__ void mgs_cols(float* X, int l, int rows, int stride) {
   }
 }
 
+template <int P>
 __global__ void __launch_bounds__(kBT) build_kernel(const BuildArgs a) {
   extern __shared__ __align__(16) uint8_t dyn[];
-  BuildSmem& s = *reinterpret_cast<BuildSmem*>(dyn);
+  BuildSmem<P>& s = *reinterpret_cast<BuildSmem<P>*>(dyn);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, c = lane & 3;
   const int item = blockIdx.x;
   const int page_i = item / a.num_kv_heads, hkv = item % a.num_kv_heads;
   const int r = a.rank;
-  const int l = min(r + 8, kLmax);
+  const int l = min(min(r + 8, kLmax), P);  // even: r and P are
 
   const int phys = a.page_ids[page_i];
   if (phys < 0 || phys >= a.pages_total) {
@@ -119,10 +126,10 @@ __global__ void __launch_bounds__(kBT) build_kernel(const BuildArgs a) {
     return;
   }
   const size_t ph = (size_t)phys * a.num_kv_heads + hkv;
-  const uint16_t* kg = a.k_pool + ph * kPage * kHeadDim;
+  const uint16_t* kg = a.k_pool + ph * P * kHeadDim;
 
   // 0. K -> shared memory (bf16, padded rows)
-  for (int e = tid; e < kPage * kHeadDim / 8; e += kBT) {
+  for (int e = tid; e < P * kHeadDim / 8; e += kBT) {
     const int row = e / 16, col = (e % 16) * 8;
     *reinterpret_cast<uint4*>(&s.K[row * kKS + col]) = __ldg(reinterpret_cast<const uint4*>(kg + row * kHeadDim + col));
   }
@@ -131,14 +138,25 @@ __global__ void __launch_bounds__(kBT) build_kernel(const BuildArgs a) {
     __syncthreads();  // K is in shared memory
     for (int dd = tid; dd < kHeadDim; dd += kBT) {
       float acc = 0.f;
-      for (int i = 0; i < kPage; ++i) acc += __bfloat162float(__ushort_as_bfloat16(s.K[i * kKS + dd]));
-      s.mu[dd] = acc * (1.f / kPage);
+      for (int i = 0; i < P; ++i) acc += __bfloat162float(__ushort_as_bfloat16(s.K[i * kKS + dd]));
+      s.mu[dd] = acc * (1.f / P);
     }
   }
   __syncthreads();
 
   // 1. A = K K^T : warp w -> rows 16*(w/2).., columns 32*(w%2)..
-  {
+  // (16-token pages: a 16 x 16 product, one entry per thread in fp32 FMAs;
+  // the bf16 products are exact in fp32 either way)
+  if constexpr (P != 64) {
+    for (int e = tid; e < P * P; e += kBT) {
+      const int i = e / P, j = e % P;
+      float acc = 0.f;
+      for (int k = 0; k < kHeadDim; ++k)
+        acc = fmaf(__bfloat162float(__ushort_as_bfloat16(s.K[i * kKS + k])),
+                   __bfloat162float(__ushort_as_bfloat16(s.K[j * kKS + k])), acc);
+      s.A[i * kAS<P> + j] = acc;
+    }
+  } else {
     const int mt = warp >> 1, nb = (warp & 1) * 4;
     float acc[4][4] = {};
     const uint32_t kbase = smem_u32(s.K);
@@ -165,36 +183,36 @@ __global__ void __launch_bounds__(kBT) build_kernel(const BuildArgs a) {
     for (int nt = 0; nt < 4; ++nt) {
       const int col = 8 * (nb + nt) + 2 * c;
       const int row = 16 * mt + g;
-      s.A[row * kAS + col] = acc[nt][0];
-      s.A[row * kAS + col + 1] = acc[nt][1];
-      s.A[(row + 8) * kAS + col] = acc[nt][2];
-      s.A[(row + 8) * kAS + col + 1] = acc[nt][3];
+      s.A[row * kAS<P> + col] = acc[nt][0];
+      s.A[row * kAS<P> + col + 1] = acc[nt][1];
+      s.A[(row + 8) * kAS<P> + col] = acc[nt][2];
+      s.A[(row + 8) * kAS<P> + col + 1] = acc[nt][3];
     }
   }
   __syncthreads();
   if (q4) {
     // Gram matrix of the centred keys: remove the row and column means
-    for (int i = tid; i < kPage; i += kBT) {
+    for (int i = tid; i < P; i += kBT) {
       float acc = 0.f;
-      for (int j = 0; j < kPage; ++j) acc += s.A[i * kAS + j];
-      s.rm[i] = acc * (1.f / kPage);
+      for (int j = 0; j < P; ++j) acc += s.A[i * kAS<P> + j];
+      s.rm[i] = acc * (1.f / P);
     }
     __syncthreads();
     if (tid == 0) {
       float acc = 0.f;
-      for (int i = 0; i < kPage; ++i) acc += s.rm[i];
-      s.grand = acc * (1.f / kPage);
+      for (int i = 0; i < P; ++i) acc += s.rm[i];
+      s.grand = acc * (1.f / P);
     }
     __syncthreads();
-    for (int e = tid; e < kPage * kPage; e += kBT) {
-      const int i = e / kPage, j = e % kPage;
-      s.A[i * kAS + j] = s.A[i * kAS + j] - s.rm[i] - s.rm[j] + s.grand;
+    for (int e = tid; e < P * P; e += kBT) {
+      const int i = e / P, j = e % P;
+      s.A[i * kAS<P> + j] = s.A[i * kAS<P> + j] - s.rm[i] - s.rm[j] + s.grand;
     }
     __syncthreads();
   }
 
   // 2. subspace iteration.  Start: A * (fixed +-1 pattern).
-  for (int e = tid; e < kPage * l; e += kBT) {
+  for (int e = tid; e < P * l; e += kBT) {
     const int i = e / l, j = e % l;
     uint32_t h = (uint32_t)(i * 131 + j * 71 + 17);
     h ^= h >> 7;
@@ -206,14 +224,14 @@ __global__ void __launch_bounds__(kBT) build_kernel(const BuildArgs a) {
   mul_A(s, s.Y, s.X, l);
   __syncthreads();
   for (int itn = 0; itn < kPowerIters; ++itn) {
-    mgs_cols(s.X, l, kPage, kXS);
+    mgs_cols(s.X, l, P, kXS);
     mul_A(s, s.X, s.Y, l);
     __syncthreads();
-    for (int e = tid; e < kPage * l; e += kBT) s.X[(e / l) * kXS + e % l] = s.Y[(e / l) * kXS + e % l];
+    for (int e = tid; e < P * l; e += kBT) s.X[(e / l) * kXS + e % l] = s.Y[(e / l) * kXS + e % l];
     __syncthreads();
   }
-  mgs_cols(s.X, l, kPage, kXS);
-  mgs_cols(s.X, l, kPage, kXS);  // twice: orthonormal to working precision
+  mgs_cols(s.X, l, P, kXS);
+  mgs_cols(s.X, l, P, kXS);  // twice: orthonormal to working precision
   mul_A(s, s.X, s.Y, l);
   __syncthreads();
 
@@ -221,7 +239,7 @@ __global__ void __launch_bounds__(kBT) build_kernel(const BuildArgs a) {
   for (int e = tid; e < l * l; e += kBT) {
     const int i = e / l, j = e % l;
     float t1 = 0.f, t2 = 0.f;
-    for (int k = 0; k < kPage; ++k) {
+    for (int k = 0; k < P; ++k) {
       t1 = fmaf(s.X[k * kXS + i], s.Y[k * kXS + j], t1);
       t2 = fmaf(s.X[k * kXS + j], s.Y[k * kXS + i], t2);
     }
@@ -309,7 +327,7 @@ __global__ void __launch_bounds__(kBT) build_kernel(const BuildArgs a) {
   __syncthreads();
 
   // U_r = X Z[:, order[0..r)]  -> stored in Y (64 x r)
-  for (int e = tid; e < kPage * r; e += kBT) {
+  for (int e = tid; e < P * r; e += kBT) {
     const int i = e / r, j = e % r;
     const int col = s.order[j];
     float acc = 0.f;
@@ -322,7 +340,7 @@ __global__ void __launch_bounds__(kBT) build_kernel(const BuildArgs a) {
   if (q4) {
     for (int j = warp; j < r; j += kBW) {
       float acc = 0.f;
-      for (int i = lane; i < kPage; i += 32) acc += s.Y[i * kXS + j];
+      for (int i = lane; i < P; i += 32) acc += s.Y[i * kXS + j];
       acc = warp_sum(acc);
       if (lane == 0) s.cs[j] = acc;
     }
@@ -331,7 +349,7 @@ __global__ void __launch_bounds__(kBT) build_kernel(const BuildArgs a) {
   for (int e = tid; e < kHeadDim * r; e += kBT) {
     const int dd = e % kHeadDim, j = e / kHeadDim;
     float acc = 0.f;
-    for (int i = 0; i < kPage; ++i)
+    for (int i = 0; i < P; ++i)
       acc = fmaf(__bfloat162float(__ushort_as_bfloat16(s.K[i * kKS + dd])), s.Y[i * kXS + j], acc);
     if (q4) acc -= s.mu[dd] * s.cs[j];
     s.V[j * kVS + dd] = acc;
@@ -371,7 +389,7 @@ __global__ void __launch_bounds__(kBT) build_kernel(const BuildArgs a) {
     }
     __syncthreads();
   }
-  for (int e = tid; e < kPage * r; e += kBT) {
+  for (int e = tid; e < P * r; e += kBT) {
     const int i = e / r, j = e % r;
     float acc = 0.f;
     for (int k = 0; k < kHeadDim; ++k)
@@ -389,7 +407,7 @@ __global__ void __launch_bounds__(kBT) build_kernel(const BuildArgs a) {
       float av = 0.f, ac = 0.f;
       if (j < r) {
         for (int k = lane; k < kHeadDim; k += 32) av = fmaxf(av, fabsf(s.V[j * kVS + k]));
-        for (int i = lane; i < kPage; i += 32) ac = fmaxf(ac, fabsf(s.Y[i * kXS + j]));
+        for (int i = lane; i < P; i += 32) ac = fmaxf(ac, fabsf(s.Y[i * kXS + j]));
       } else {
         for (int k = lane; k < kHeadDim; k += 32) ac = fmaxf(ac, fabsf(s.mu[k]));
       }
@@ -408,7 +426,7 @@ __global__ void __launch_bounds__(kBT) build_kernel(const BuildArgs a) {
     auto code = [](float x, float sc, float qmax) -> int {
       return sc > 0.f ? (int)fminf(fmaxf(rintf(x / sc), -qmax), qmax) : 0;
     };
-    uint8_t* blk = static_cast<uint8_t*>(a.basis_t) + ph * (size_t)LOCKS_Q4_PAGE_HEAD_BYTES(r);
+    uint8_t* blk = static_cast<uint8_t*>(a.basis_t) + ph * (size_t)LOCKS_Q4_BLOCK_BYTES(r, P);
     // basis: word m of row j holds elements 8m .. 8m+7, element 8m+i at
     // bits 4(i/2) + 16(i%2), as code + 8
     uint32_t* bw = reinterpret_cast<uint32_t*>(blk);
@@ -421,34 +439,43 @@ __global__ void __launch_bounds__(kBT) build_kernel(const BuildArgs a) {
       bw[e] = w;
     }
     for (int k = tid; k < kHeadDim; k += kBT) blk[64 * r + k] = (uint8_t)(code(s.mu[k], s.smu, 127.f) + 128);
-    for (int e = tid; e < kPage * r; e += kBT)
+    for (int e = tid; e < P * r; e += kBT)
       blk[64 * r + kHeadDim + e] = (uint8_t)(code(s.Y[(e / r) * kXS + e % r], s.sc[e % r], 127.f) + 128);
-    float* sco = reinterpret_cast<float*>(blk + 128 * r + kHeadDim);
+    float* sco = reinterpret_cast<float*>(blk + 64 * r + kHeadDim + P * r);
     for (int e = tid; e < 2 * r + 1; e += kBT) sco[e] = e < r ? s.sv[e] : (e < 2 * r ? s.sc[e - r] : s.smu);
   } else if (a.format == LOCKS_DTYPE_F32) {
     float* bo = reinterpret_cast<float*>(a.basis_t) + ph * (size_t)r * kHeadDim;
-    float* co = reinterpret_cast<float*>(a.coeffs) + ph * (size_t)kPage * r;
+    float* co = reinterpret_cast<float*>(a.coeffs) + ph * (size_t)P * r;
     for (int e = tid; e < r * kHeadDim; e += kBT) bo[e] = s.V[(e / kHeadDim) * kVS + e % kHeadDim];
-    for (int e = tid; e < kPage * r; e += kBT) co[e] = s.Y[(e / r) * kXS + e % r];
+    for (int e = tid; e < P * r; e += kBT) co[e] = s.Y[(e / r) * kXS + e % r];
   } else {
     uint16_t* bo = reinterpret_cast<uint16_t*>(a.basis_t) + ph * (size_t)r * kHeadDim;
-    uint16_t* co = reinterpret_cast<uint16_t*>(a.coeffs) + ph * (size_t)kPage * r;
+    uint16_t* co = reinterpret_cast<uint16_t*>(a.coeffs) + ph * (size_t)P * r;
     for (int e = tid; e < r * kHeadDim; e += kBT)
       bo[e] = __bfloat16_as_ushort(__float2bfloat16_rn(s.V[(e / kHeadDim) * kVS + e % kHeadDim]));
-    for (int e = tid; e < kPage * r; e += kBT)
+    for (int e = tid; e < P * r; e += kBT)
       co[e] = __bfloat16_as_ushort(__float2bfloat16_rn(s.Y[(e / r) * kXS + e % r]));
   }
 }
 
 }  // namespace
 
+namespace {
+
+template <int P>
+cudaError_t launch_page(const BuildArgs& a, cudaStream_t st) {
+  const size_t smem = sizeof(BuildSmem<P>);
+  cudaError_t e = cudaFuncSetAttribute(build_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  build_kernel<P><<<dim3(a.n * a.num_kv_heads), dim3(kBT), smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
 cudaError_t launch_build(const BuildArgs& a, cudaStream_t st) {
   if (a.n <= 0) return cudaSuccess;
-  const size_t smem = sizeof(BuildSmem);
-  cudaError_t e = cudaFuncSetAttribute(build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  build_kernel<<<dim3(a.n * a.num_kv_heads), dim3(kBT), smem, st>>>(a);
-  return cudaGetLastError();
+  return a.page_size == 16 ? launch_page<16>(a, st) : launch_page<kPage>(a, st);
 }
 
 }  // namespace locks

@@ -23,6 +23,7 @@ struct ScanArgs {
   int chunk_pages, n_chunks;
   float scale_log2;            // scale * log2(e)
   int q4;                      // 1: basis_t holds LOCKS_DTYPE_Q4 blocks (coeffs unused)
+  int page_size;               // P: 64 or 16
 };
 
 // GSA scores + top-k (chunk-local candidates, merged by the last CTA).
@@ -41,6 +42,7 @@ struct TopkArgs {
   int batch, num_kv_heads, group, max_pages, k_max;
   int chunk_pages, n_chunks;
   size_t smem_keys;     // capacity (entries) of the dynamic key buffer
+  int page_size;
 };
 
 // Paged flash-decode over a page list (sparse), every page (dense), or the
@@ -64,6 +66,7 @@ struct AttendArgs {
   int cluster;                // CTAs per thread-block cluster (1 in page-LSE mode)
   int inputs_early;           // 1: the step's inputs may be read before the grid dependency wait
   float scale_log2;
+  int page_size;              // P: 64 (one page per 64-token tile) or 16 (four pages per tile)
 };
 
 enum AttendMode { kAttendSparse = 0, kAttendDense = 1, kAttendPageLse = 2 };
@@ -77,6 +80,7 @@ struct BuildArgs {
   int n, num_kv_heads, rank, pages_total;
   int format;  // LOCKS_DTYPE_BF16 / _F32 (basis_t + coeffs) or _Q4 (packed blocks in basis_t)
   int* err;
+  int page_size;
 };
 
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s, bool pdl);
@@ -87,8 +91,8 @@ cudaError_t launch_build(const BuildArgs& a, cudaStream_t s);
 
 size_t topk_smem_bytes(size_t keys);
 int topk_pages_per_cta(int group);  // pages one top-k CTA scores
-int attend_max_cluster(int mode);  // largest placeable cluster (<= 16) for that mode
-int attend_active_clusters(int mode, int cs);  // clusters of cs CTAs resident at once
+int attend_max_cluster(int mode, int page_size);  // largest placeable cluster (<= 16) for that mode
+int attend_active_clusters(int mode, int cs, int page_size);  // clusters of cs CTAs resident at once
 // Scan CTA: 7 consumer warps + 1 producer warp, so that two CTAs put four
 // warps on each SM sub-partition (whose register file is a quarter of the SM's).
 constexpr int kScanWarps = 7;

@@ -32,7 +32,11 @@
 //       tolerance) so the second product keeps most of fp32's accuracy.  The
 //       accumulator of (1) is already in the A-fragment layout of (2);
 //       n-tile jt, column g is token 8*jt + g.
-// Then a base-2 log-sum-exp over the 64 tokens per head.  Each CTA also
+// Then a base-2 log-sum-exp over the P tokens per head (P = 64 or 16; at 16
+// the first contraction is the same and the second one a quarter as long, so
+// a page-head costs nearly as much as at 64 while covering a quarter of the
+// tokens: the explainer's §2 "Kernmechanisme" notes that the summary is
+// then about 10% of the page's KV bytes).  Each CTA also
 // reduces its pages' s_hat into a per-head (max, sum) pair, from which the
 // top-k kernel gets the total estimated mass Z_h of each head without
 // re-reading every s_hat.
@@ -129,10 +133,11 @@ __device__ __forceinline__ float lse2_lanes(float* v) {
 //
 // Page-head in shared memory at `slot` -> base-2 LSE for head g (e0) and,
 // with G16, head g + 8 (e1).
-template <bool G16, bool R16, bool GRP2>
+template <bool G16, bool R16, bool GRP2, int P>
 __device__ __forceinline__ void compute_page(uint32_t slot, const uint4 (&qa)[4], const uint4 (&qb)[4], int r,
                                              float scale_log2, int lane, float& e0, float& e1) {
   using RG = Ring<R16>;
+  constexpr int NT = P / 8;  // 8-token n-tiles of the page
   const int g = lane >> 2, c = lane & 3;
   const uint4 z4 = make_uint4(0, 0, 0, 0);
   // basis row `row`, 16-byte piece d = 32*s + 8c (linear rows of 256 B)
@@ -170,18 +175,20 @@ __device__ __forceinline__ void compute_page(uint32_t slot, const uint4 (&qa)[4]
     const bool lo_half = lane < 16;
     const uint32_t ha0 = lo_half ? hh : 0u, ha2 = lo_half ? 0u : hh;
     const uint32_t ma0 = lo_half ? mm : 0u, ma2 = lo_half ? 0u : mm;
-    uint32_t cbv[8];
+    uint32_t cbv[NT];
 #pragma unroll
-    for (int jt = 0; jt < 8; ++jt) cbv[jt] = (2 * c < r) ? lds32(coef_word(jt, 2 * c)) : 0u;
-    float d[4][4];
+    for (int jt = 0; jt < NT; ++jt) cbv[jt] = (2 * c < r) ? lds32(coef_word(jt, 2 * c)) : 0u;
+    float d[NT / 2][4];
+    float v[NT];
 #pragma unroll
-    for (int jt = 0; jt < 4; ++jt) {
+    for (int jt = 0; jt < NT / 2; ++jt) {
       d[jt][0] = d[jt][1] = d[jt][2] = d[jt][3] = 0.f;
       mma_16816(d[jt], ma0, 0u, ma2, 0u, cbv[2 * jt], cbv[2 * jt + 1]);
       mma_16816(d[jt], ha0, 0u, ha2, 0u, cbv[2 * jt], cbv[2 * jt + 1]);
+      v[2 * jt] = d[jt][0];
+      v[2 * jt + 1] = d[jt][1];
     }
-    float v[8] = {d[0][0], d[0][1], d[1][0], d[1][1], d[2][0], d[2][1], d[3][0], d[3][1]};
-    e0 = lse2_lanes<8, 1, 2, 16>(v);
+    e0 = lse2_lanes<NT, 1, 2, 16>(v);
     e1 = 0.f;
     return;
   }
@@ -194,16 +201,16 @@ __device__ __forceinline__ void compute_page(uint32_t slot, const uint4 (&qa)[4]
     split2(w1[0] * scale_log2, w1[1] * scale_log2, h2, m2);
     split2(w1[2] * scale_log2, w1[3] * scale_log2, h3, m3);
   }
-  uint32_t cb[8], cc[8];
+  uint32_t cb[NT], cc[NT];
 #pragma unroll
-  for (int jt = 0; jt < 8; ++jt) {
+  for (int jt = 0; jt < NT; ++jt) {
     cb[jt] = (2 * c < r) ? lds32(coef_word(jt, 2 * c)) : 0u;
     cc[jt] = (R16 && 2 * c + 8 < r) ? lds32(coef_word(jt, 2 * c + 8)) : 0u;
   }
-  // (2) logits (base-2) for 16 heads x 64 tokens
-  float d[8][4];
+  // (2) logits (base-2) for 16 heads x P tokens
+  float d[NT][4];
 #pragma unroll
-  for (int jt = 0; jt < 8; ++jt) {
+  for (int jt = 0; jt < NT; ++jt) {
     d[jt][0] = d[jt][1] = d[jt][2] = d[jt][3] = 0.f;
     if (R16) {
       mma_16816(d[jt], m0, m1, m2, m3, cb[jt], cc[jt]);
@@ -213,23 +220,23 @@ __device__ __forceinline__ void compute_page(uint32_t slot, const uint4 (&qa)[4]
       mma_1688(d[jt], h0, h1, cb[jt]);
     }
   }
-  // base-2 log-sum-exp over the 64 tokens of each head row (16 values per
+  // base-2 log-sum-exp over the P tokens of each head row (P / 4 values per
   // lane, four lanes per row)
-  float v[16];
+  float v[2 * NT];
 #pragma unroll
-  for (int jt = 0; jt < 8; ++jt) {
+  for (int jt = 0; jt < NT; ++jt) {
     v[2 * jt] = d[jt][0];
     v[2 * jt + 1] = d[jt][1];
   }
-  e0 = lse2_lanes<16, 1, 2, 0>(v);
+  e0 = lse2_lanes<2 * NT, 1, 2, 0>(v);
   e1 = 0.f;
   if (G16) {
 #pragma unroll
-    for (int jt = 0; jt < 8; ++jt) {
+    for (int jt = 0; jt < NT; ++jt) {
       v[2 * jt] = d[jt][2];
       v[2 * jt + 1] = d[jt][3];
     }
-    e1 = lse2_lanes<16, 1, 2, 0>(v);
+    e1 = lse2_lanes<2 * NT, 1, 2, 0>(v);
   }
 }
 
@@ -239,11 +246,12 @@ __device__ __forceinline__ void compute_page(uint32_t slot, const uint4 (&qa)[4]
 // the scales enter in fp32 -- each basis vector's and coefficient column's
 // scale on its column of W.  Returns the LSE of the centred logits; q . mu
 // shifts every logit of the head alike and is added later (mu_batch).
-template <bool G16, bool GRP2>
+template <bool G16, bool GRP2, int P>
 __device__ __forceinline__ void compute_page_q4(uint32_t slot, const uint4 (&qa)[4], const uint4 (&qb)[4], int r,
                                                 float scale_log2, int lane, float& e0, float& e1) {
+  constexpr int NT = P / 8;
   const int g = lane >> 2, c = lane & 3;
-  const uint32_t coef_off = 64 * r + kHeadDim, sc_off = 128 * r + kHeadDim;
+  const uint32_t coef_off = 64 * r + kHeadDim, sc_off = 64 * r + kHeadDim + P * r;
   // (1) W^T = Q V on the basis codes
   float w0[4] = {0.f, 0.f, 0.f, 0.f}, x0[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -274,18 +282,20 @@ __device__ __forceinline__ void compute_page_q4(uint32_t slot, const uint4 (&qa)
     const bool lo_half = lane < 16;
     const uint32_t ha0 = lo_half ? hh : 0u, ha2 = lo_half ? 0u : hh;
     const uint32_t ma0 = lo_half ? mm : 0u, ma2 = lo_half ? 0u : mm;
-    uint32_t cbv[8];
+    uint32_t cbv[NT];
 #pragma unroll
-    for (int jt = 0; jt < 8; ++jt) cbv[jt] = coef(jt);
-    float d[4][4];
+    for (int jt = 0; jt < NT; ++jt) cbv[jt] = coef(jt);
+    float d[NT / 2][4];
+    float v[NT];
 #pragma unroll
-    for (int jt = 0; jt < 4; ++jt) {
+    for (int jt = 0; jt < NT / 2; ++jt) {
       d[jt][0] = d[jt][1] = d[jt][2] = d[jt][3] = 0.f;
       mma_16816(d[jt], ma0, 0u, ma2, 0u, cbv[2 * jt], cbv[2 * jt + 1]);
       mma_16816(d[jt], ha0, 0u, ha2, 0u, cbv[2 * jt], cbv[2 * jt + 1]);
+      v[2 * jt] = d[jt][0];
+      v[2 * jt + 1] = d[jt][1];
     }
-    float v[8] = {d[0][0], d[0][1], d[1][0], d[1][1], d[2][0], d[2][1], d[3][0], d[3][1]};
-    e0 = lse2_lanes<8, 1, 2, 16>(v);
+    e0 = lse2_lanes<NT, 1, 2, 16>(v);
     e1 = 0.f;
     return;
   }
@@ -293,31 +303,31 @@ __device__ __forceinline__ void compute_page_q4(uint32_t slot, const uint4 (&qa)
   uint32_t h0, m0, h1, m1;
   split2(wa, wb, h0, m0);
   split2(wc, wd, h1, m1);
-  uint32_t cb[8];
+  uint32_t cb[NT];
 #pragma unroll
-  for (int jt = 0; jt < 8; ++jt) cb[jt] = coef(jt);
-  float d[8][4];
+  for (int jt = 0; jt < NT; ++jt) cb[jt] = coef(jt);
+  float d[NT][4];
 #pragma unroll
-  for (int jt = 0; jt < 8; ++jt) {
+  for (int jt = 0; jt < NT; ++jt) {
     d[jt][0] = d[jt][1] = d[jt][2] = d[jt][3] = 0.f;
     mma_1688(d[jt], m0, m1, cb[jt]);
     mma_1688(d[jt], h0, h1, cb[jt]);
   }
-  float v[16];
+  float v[2 * NT];
 #pragma unroll
-  for (int jt = 0; jt < 8; ++jt) {
+  for (int jt = 0; jt < NT; ++jt) {
     v[2 * jt] = d[jt][0];
     v[2 * jt + 1] = d[jt][1];
   }
-  e0 = lse2_lanes<16, 1, 2, 0>(v);
+  e0 = lse2_lanes<2 * NT, 1, 2, 0>(v);
   e1 = 0.f;
   if (G16) {
 #pragma unroll
-    for (int jt = 0; jt < 8; ++jt) {
+    for (int jt = 0; jt < NT; ++jt) {
       v[2 * jt] = d[jt][2];
       v[2 * jt + 1] = d[jt][3];
     }
-    e1 = lse2_lanes<16, 1, 2, 0>(v);
+    e1 = lse2_lanes<2 * NT, 1, 2, 0>(v);
   }
 }
 
@@ -340,7 +350,7 @@ __device__ __forceinline__ void mu_batch(uint32_t stage_mu, int nb, const uint4 
   for (int e = 0; e < 4; ++e) u[e] += y[e];
 }
 
-template <bool G16, bool R16, bool GRP2, bool Q4>
+template <bool G16, bool R16, bool GRP2, bool Q4, int P>
 __global__ void __launch_bounds__(kScanThreads, 2) scan_kernel(const ScanArgs a) {
   using RG = Ring<R16, Q4>;
   constexpr int S = RG::kSlots;
@@ -373,9 +383,9 @@ __global__ void __launch_bounds__(kScanThreads, 2) scan_kernel(const ScanArgs a)
 
   const int L = a.seq_lens[b];
   int ns = a.n_summarized[b];
-  const int nfull = L < 0 ? 0 : L / kPage;
+  const int nfull = L < 0 ? 0 : L / P;
   const int cap = nfull < a.max_pages ? nfull : a.max_pages;
-  if (ns > cap || ns < 0 || L > a.max_pages * kPage) {
+  if (ns > cap || ns < 0 || L > a.max_pages * P) {
     if (threadIdx.x == 0 && chunk == 0) set_error(a.err, LOCKS_DEVERR_LENGTHS);
     ns = ns < 0 ? 0 : (ns > cap ? cap : ns);
   }
@@ -389,8 +399,8 @@ __global__ void __launch_bounds__(kScanThreads, 2) scan_kernel(const ScanArgs a)
     // Each lane tests its own slot without blocking, so a released slot is
     // refilled at once whatever the other lanes' slots are doing.
     const int32_t* bt = a.block_table + (size_t)b * a.max_pages;
-    const size_t ph_stride_b = (size_t)r * kHeadDim, ph_stride_c = (size_t)kPage * r;
-    const uint32_t basis_bytes = (uint32_t)(r * kHeadDim * 2), coef_bytes = (uint32_t)(kPage * r * 2);
+    const size_t ph_stride_b = (size_t)r * kHeadDim, ph_stride_c = (size_t)P * r;
+    const uint32_t basis_bytes = (uint32_t)(r * kHeadDim * 2), coef_bytes = (uint32_t)(P * r * 2);
     // the block-table entries of this lane's first kPre pages, read up front
     constexpr int kPre = 8;
     int pre[kPre];
@@ -421,7 +431,7 @@ __global__ void __launch_bounds__(kScanThreads, 2) scan_kernel(const ScanArgs a)
           const uint32_t slot = ring + lane * RG::kSlot;
           if (Q4) {
             // one packed block per page-head
-            const uint32_t qbytes = (uint32_t)LOCKS_Q4_PAGE_HEAD_BYTES(r);
+            const uint32_t qbytes = (uint32_t)LOCKS_Q4_BLOCK_BYTES(r, P);
             mbar_arrive_expect_tx(&full_bar[lane], qbytes);
             bulk_load(slot, reinterpret_cast<const uint8_t*>(a.basis_t) + ph * qbytes, qbytes, &full_bar[lane]);
           } else {
@@ -510,15 +520,15 @@ __global__ void __launch_bounds__(kScanThreads, 2) scan_kernel(const ScanArgs a)
       float e0 = 0.f, e1 = 0.f;
       if (valid) {
         if (Q4)
-          compute_page_q4<G16, GRP2>(ring + s * RG::kSlot, qa, qb, r, a.scale_log2, lane, e0, e1);
+          compute_page_q4<G16, GRP2, P>(ring + s * RG::kSlot, qa, qb, r, a.scale_log2, lane, e0, e1);
         else
-          compute_page<G16, R16, GRP2>(ring + s * RG::kSlot, qa, qb, r, a.scale_log2, lane, e0, e1);
+          compute_page<G16, R16, GRP2, P>(ring + s * RG::kSlot, qa, qb, r, a.scale_log2, lane, e0, e1);
       }
       if (Q4 && valid) {
         // stage the centroid codes (one word per lane), its scale and the LSEs
         const uint32_t slot = ring + s * RG::kSlot;
         sts32(st_mu + 128 * npend + 4 * lane, lds32(slot + 64 * r + 4 * lane));
-        if (lane == 0) st_smu[npend] = __uint_as_float(lds32(slot + 128 * r + kHeadDim + 8 * r));
+        if (lane == 0) st_smu[npend] = __uint_as_float(lds32(slot + 64 * r + kHeadDim + P * r + 8 * r));
         if (c == 0) {
           st_pend[npend * 16 + g] = e0;
           if (G16) st_pend[npend * 16 + g + 8] = e1;
@@ -585,11 +595,11 @@ __global__ void __launch_bounds__(kScanThreads, 2) scan_kernel(const ScanArgs a)
   trace_mark(a.err, kTrScanExit, false);
 }
 
-template <bool G16, bool R16, bool GRP2, bool Q4 = false>
+template <bool G16, bool R16, bool GRP2, bool Q4, int P>
 cudaError_t launch_one(const ScanArgs& a, cudaStream_t s, bool pdl) {
   const int smem = scan_smem_bytes<R16, Q4>();
   cudaError_t e =
-      cudaFuncSetAttribute(scan_kernel<G16, R16, GRP2, Q4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      cudaFuncSetAttribute(scan_kernel<G16, R16, GRP2, Q4, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_chunks, a.batch * a.num_kv_heads, 1);
@@ -601,22 +611,28 @@ cudaError_t launch_one(const ScanArgs& a, cudaStream_t s, bool pdl) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, scan_kernel<G16, R16, GRP2, Q4>, a);
+  return cudaLaunchKernelEx(&cfg, scan_kernel<G16, R16, GRP2, Q4, P>, a);
+}
+
+template <int P>
+cudaError_t launch_page(const ScanArgs& a, cudaStream_t s, bool pdl) {
+  const bool g16 = a.group > 8, r16 = a.rank > 8;
+  if (a.q4) {  // rank <= 8 (checked by the caller)
+    if (g16) return launch_one<true, false, false, true, P>(a, s, pdl);
+    if (a.group <= 4) return launch_one<false, false, true, true, P>(a, s, pdl);
+    return launch_one<false, false, false, true, P>(a, s, pdl);
+  }
+  if (g16)
+    return r16 ? launch_one<true, true, false, false, P>(a, s, pdl) : launch_one<true, false, false, false, P>(a, s, pdl);
+  if (r16) return launch_one<false, true, false, false, P>(a, s, pdl);
+  if (a.group <= 4) return launch_one<false, false, true, false, P>(a, s, pdl);
+  return launch_one<false, false, false, false, P>(a, s, pdl);
 }
 
 }  // namespace
 
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s, bool pdl) {
-  const bool g16 = a.group > 8, r16 = a.rank > 8;
-  if (a.q4) {  // rank <= 8 (checked by the caller)
-    if (g16) return launch_one<true, false, false, true>(a, s, pdl);
-    if (a.group <= 4) return launch_one<false, false, true, true>(a, s, pdl);
-    return launch_one<false, false, false, true>(a, s, pdl);
-  }
-  if (g16) return r16 ? launch_one<true, true, false>(a, s, pdl) : launch_one<true, false, false>(a, s, pdl);
-  if (r16) return launch_one<false, true, false>(a, s, pdl);
-  if (a.group <= 4) return launch_one<false, false, true>(a, s, pdl);
-  return launch_one<false, false, false>(a, s, pdl);
+  return a.page_size == 16 ? launch_page<16>(a, s, pdl) : launch_page<kPage>(a, s, pdl);
 }
 
 }  // namespace locks

@@ -458,7 +458,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkArgs a)
     }
   }
 
-  const int nfull = L < 0 ? 0 : L / kPage;
+  const int nfull = L < 0 ? 0 : L / a.page_size;
   const int cap = nfull < a.max_pages ? nfull : a.max_pages;
   ns = ns < 0 ? 0 : (ns > cap ? cap : ns);
   const int k = ns < a.k_max ? ns : a.k_max;

@@ -31,9 +31,9 @@ LOCKS_DTYPE_F32 = 1
 LOCKS_DTYPE_Q4 = 2
 
 
-def q4_page_head_bytes(rank: int) -> int:
-    """Bytes of one page-head of a LOCKS_DTYPE_Q4 summary (LOCKS_Q4_PAGE_HEAD_BYTES)."""
-    return (136 * rank + 132 + 15) // 16 * 16
+def q4_page_head_bytes(rank: int, page_size: int = 64) -> int:
+    """Bytes of one page-head of a LOCKS_DTYPE_Q4 summary (LOCKS_Q4_BLOCK_BYTES)."""
+    return (72 * rank + page_size * rank + 132 + 15) // 16 * 16
 LOCKS_DEVERR_BLOCK_TABLE = 0x1
 LOCKS_DEVERR_SEL_PAGE = 0x2
 LOCKS_DEVERR_LENGTHS = 0x4

@@ -15,11 +15,11 @@ from . import locks as L
 class LocksRuntime:
     """Holds a paged cache on ``device`` and calls liblocks.so on it.
 
-    k_pool, v_pool: bf16 [pages_total][Hkv][64][128]; block_table int32
-    [B][max_pages]; seq_lens, n_summarized int32 [B].  Summaries are
-    allocated here: bf16 [pages_total][Hkv][rank][128] and [..][64][rank],
-    or, with ``quantized``, one packed LOCKS_DTYPE_Q4 block per page-head
-    (uint8 [pages_total][Hkv][q4_page_head_bytes(rank)]).
+    k_pool, v_pool: bf16 [pages_total][Hkv][P][128] with P = 64 or 16;
+    block_table int32 [B][max_pages]; seq_lens, n_summarized int32 [B].
+    Summaries are allocated here: bf16 [pages_total][Hkv][rank][128] and
+    [..][P][rank], or, with ``quantized``, one packed LOCKS_DTYPE_Q4 block per
+    page-head (uint8 [pages_total][Hkv][q4_page_head_bytes(rank, P)]).
     """
 
     def __init__(self, k_pool: torch.Tensor, v_pool: torch.Tensor, block_table: torch.Tensor,
@@ -37,7 +37,8 @@ class LocksRuntime:
         self.rank = rank
         self.quantized = quantized
         if quantized:
-            self.basis_t = torch.zeros((pt, hkv, L.q4_page_head_bytes(rank)), dtype=torch.uint8, device=self.device)
+            self.basis_t = torch.zeros((pt, hkv, L.q4_page_head_bytes(rank, P)), dtype=torch.uint8,
+                                       device=self.device)
             self.coeffs = None
         else:
             self.basis_t = torch.zeros((pt, hkv, rank, d), dtype=torch.bfloat16, device=self.device)

@@ -251,7 +251,7 @@ def make_config_case(name: str, *, context: int | None = None, batch: int | None
     case = make_case(cfg["batch"], cfg["num_q_heads"], cfg["num_kv_heads"], cfg["context"],
                      true_rank=cfg["true_rank"], n_carriers=cfg["n_carriers"], drift=cfg["drift"],
                      seed=cfg["seed"], spare_pages=cfg.get("spare_pages", 0),
-                     max_pages=cfg.get("max_pages"))
+                     max_pages=cfg.get("max_pages"), page_size=cfg.get("page_size", PAGE_SIZE))
     return case, cfg
 
 

@@ -30,19 +30,27 @@ def oracle_summaries_bf16(case, r: int, pages=None):
     return basis_t, coeffs
 
 
+def q4_block_bytes(r: int, P: int = 64) -> int:
+    """LOCKS_Q4_BLOCK_BYTES(r, P): 64r basis + 128 centroid + P r coefficients
+    + 4 (2r + 1) scales, rounded up to 16."""
+    return (64 * r + 128 + P * r + 4 * (2 * r + 1) + 15) // 16 * 16
+
+
 def pack_q4(qs: dict, r: int) -> np.ndarray:
-    """One oracle-quantised page-head summary in the LOCKS_DTYPE_Q4 byte layout."""
-    nbytes = (136 * r + 132 + 15) // 16 * 16
-    buf = np.zeros(nbytes, dtype=np.uint8)
+    """One oracle-quantised page-head summary in the LOCKS_DTYPE_Q4 byte layout
+    (the page size is the coefficient block's row count)."""
+    P = np.asarray(qs["cq"]).shape[0]
+    buf = np.zeros(q4_block_bytes(r, P), dtype=np.uint8)
     u = (np.asarray(qs["vq"]) + 8).astype(np.uint32).reshape(r, 16, 8)  # [row][word][element], code + 8
     words = np.zeros((r, 16), dtype=np.uint32)
     for i in range(8):
         words |= u[:, :, i] << np.uint32(4 * (i // 2) + 16 * (i % 2))
     buf[:64 * r] = words.astype("<u4").view(np.uint8).reshape(-1)
     buf[64 * r:64 * r + 128] = (np.asarray(qs["muq"]) + 128).astype(np.uint8)
-    buf[64 * r + 128:128 * r + 128] = (np.asarray(qs["cq"]) + 128).astype(np.uint8).reshape(-1)
+    c0 = 64 * r + 128
+    buf[c0:c0 + P * r] = (np.asarray(qs["cq"]) + 128).astype(np.uint8).reshape(-1)
     scales = np.concatenate([qs["sv"], qs["sc"], [qs["smu"]]]).astype(np.float32)
-    buf[128 * r + 128:128 * r + 128 + 4 * (2 * r + 1)] = scales.view(np.uint8)
+    buf[c0 + P * r:c0 + P * r + 4 * (2 * r + 1)] = scales.view(np.uint8)
     return buf
 
 
@@ -55,8 +63,9 @@ def unpack_q4(buf: np.ndarray, r: int, P: int = 64, d: int = 128) -> dict:
         vq[:, :, i] = ((words >> (4 * (i // 2) + 16 * (i % 2))) & 15) - 8
     vq = vq.reshape(r, d)
     muq = buf[64 * r:64 * r + 128].astype(np.int64) - 128
-    cq = (buf[64 * r + 128:128 * r + 128].astype(np.int64) - 128).reshape(P, r)
-    sc = buf[128 * r + 128:128 * r + 128 + 4 * (2 * r + 1)].view(np.float32).astype(np.float64)
+    c0 = 64 * r + 128
+    cq = (buf[c0:c0 + P * r].astype(np.int64) - 128).reshape(P, r)
+    sc = buf[c0 + P * r:c0 + P * r + 4 * (2 * r + 1)].view(np.float32).astype(np.float64)
     return dict(vq=vq, sv=sc[:r], cq=cq, sc=sc[r:2 * r], muq=muq, smu=float(sc[2 * r]))
 
 
@@ -66,8 +75,7 @@ def oracle_summaries_q4(case, r: int, heads=None, pages=None):
     array uint8 [pages_total][Hkv][bytes] and the values it stands for in the
     oracle layout (basis [..][d][r], coeffs [..][P][r], centroid [..][d])."""
     pt, hkv, P, d = case.k_pool.shape
-    nbytes = (136 * r + 132 + 15) // 16 * 16
-    packed = np.zeros((pt, hkv, nbytes), dtype=np.uint8)
+    packed = np.zeros((pt, hkv, q4_block_bytes(r, P)), dtype=np.uint8)
     basis = np.zeros((pt, hkv, d, r))
     coeffs = np.zeros((pt, hkv, P, r))
     cent = np.zeros((pt, hkv, d))

@@ -5,11 +5,14 @@ the documented status codes before launching anything."""
 import ctypes
 import os
 import subprocess
+from pathlib import Path
 
 import pytest
 
 from sparse_kv_page_rank_gb300 import locks as L
 from sparse_kv_page_rank_gb300.build_lib import LIB, build
+
+ROOT = Path(__file__).resolve().parents[1]
 
 
 @pytest.fixture(scope="module")
@@ -48,6 +51,31 @@ def _cache(**kw):
     return L.locks_cache_t(**d)
 
 
+def test_sixteen_token_pages_accepted(lib):
+    p = L.make_params(8, 512)
+    a = L.locks_workspace_size(_cache(page_size=16, max_pages=40, pages_total=40), None, p)
+    b = L.locks_workspace_size(_cache(page_size=64), None, p)
+    # four times the pages per token budget: more selected pages, more candidates
+    assert a > b > 0 and a % 256 == 0
+
+
+def _header_q4_block_bytes(r, P):
+    """Evaluates LOCKS_Q4_BLOCK_BYTES as written in include/locks.h."""
+    import re
+    text = (ROOT / "include" / "locks.h").read_text()
+    m = re.search(r"#define LOCKS_Q4_BLOCK_BYTES\(r, P\) (.+)", text)
+    expr = m.group(1).replace("(r)", str(r)).replace("(P)", str(P)).replace("/", "//")
+    return eval(expr)
+
+
+@pytest.mark.parametrize("r", [2, 4, 6, 8])
+@pytest.mark.parametrize("P", [16, 64])
+def test_q4_block_bytes_agree(r, P):
+    from helpers import q4_block_bytes
+    assert _header_q4_block_bytes(r, P) == L.q4_page_head_bytes(r, P) == q4_block_bytes(r, P)
+    assert L.q4_page_head_bytes(r, P) % 16 == 0
+
+
 def test_workspace_size_grows_with_shapes(lib):
     p = L.make_params(8, 512)
     a = L.locks_workspace_size(_cache(), None, p)
@@ -57,7 +85,7 @@ def test_workspace_size_grows_with_shapes(lib):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(head_dim=64), L.LOCKS_ERR_UNSUPPORTED),
-    (dict(page_size=16), L.LOCKS_ERR_UNSUPPORTED),
+    (dict(page_size=32), L.LOCKS_ERR_UNSUPPORTED),
     (dict(batch=0), L.LOCKS_ERR_INVALID_ARG),
     (dict(max_pages=0), L.LOCKS_ERR_INVALID_ARG),
 ])

@@ -30,6 +30,17 @@ def test_residency_matches_pages(name):
     assert _close(_residency(f["format"]), f["value"], f["rel_tol"])
 
 
+@pytest.mark.parametrize("name", ["residency_r8", "residency_r2"])
+def test_library_q4_block_matches_pages(name):
+    # the library's LOCKS_DTYPE_Q4 block at the pages' page size, against the
+    # page's own K + V bytes
+    from sparse_kv_page_rank_gb300.locks import q4_page_head_bytes
+    f = FIG[name]
+    fmt = f["format"]
+    kv = 2 * fmt["page"] * fmt["head_dim"] * 2
+    assert _close(q4_page_head_bytes(fmt["rank"], fmt["page"]) / kv, f["value"], f["rel_tol"])
+
+
 def _reduction(rank, context, budget):
     # per page-head: dense reads K+V of every token; the step reads every
     # summary (quantised format) plus K+V of the budget's tokens

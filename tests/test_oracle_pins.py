@@ -137,12 +137,13 @@ def test_centered_summary_identical_keys_closed_form():
     assert abs(O.reconstructed_page_lse(q, V, C, mu) - (math.log(P) + q @ k / math.sqrt(d))) < 1e-12
 
 
+@pytest.mark.parametrize("P", [64, 16])
 @pytest.mark.parametrize("centered", [False, True])
-def test_full_rank_reconstruction_equals_exact_lse(centered):
+def test_full_rank_reconstruction_equals_exact_lse(centered, P):
     """At r = min(P, d) the reconstructed page LSE equals the exact LSE that
     reads every key (equation for s_hat_j(q), explainer §2), to 1e-12."""
     rng = np.random.default_rng(5)
-    P, d = 64, 128
+    d = 128
     K = rng.standard_normal((P, d)) * 2
     for _ in range(5):
         q = rng.standard_normal(d) * 3
@@ -246,14 +247,15 @@ def test_attention_uniform_keys_mean_value():
     assert np.allclose(o, V.mean(axis=0)[None, :], atol=1e-13)
 
 
-def _small_case(seed=9, G=2, Hkv=2, L=64 * 21 + 17, B=2):
-    return make_case(B, G * Hkv, Hkv, [L, L - 64 * 3 - 5][:B], true_rank=(2, 8), n_carriers=2, seed=seed)
+def _small_case(seed=9, G=2, Hkv=2, L=64 * 21 + 17, B=2, P=64):
+    return make_case(B, G * Hkv, Hkv, [L, L - 64 * 3 - 5][:B], true_rank=(2, 8), n_carriers=2, seed=seed,
+                     page_size=P)
 
 
 def _oracle_summaries(case, r):
     kf = O.bf16_widen(case.k_pool)
     basis = np.zeros((case.pages_total, case.num_kv_heads, 128, r))
-    coeffs = np.zeros((case.pages_total, case.num_kv_heads, 64, r))
+    coeffs = np.zeros((case.pages_total, case.num_kv_heads, case.page_size, r))
     for b in range(case.batch):
         for j in range(case.n_full_pages(b)):
             p = case.block_table[b, j]
@@ -263,28 +265,30 @@ def _oracle_summaries(case, r):
     return basis, coeffs
 
 
-def test_budget_covering_all_pages_equals_dense():
+@pytest.mark.parametrize("P", [64, 16])
+def test_budget_covering_all_pages_equals_dense(P):
     """Selecting every page reads the whole cache: the output is dense attention."""
-    case = _small_case()
+    case = _small_case(P=P)
     basis, coeffs = _oracle_summaries(case, 4)
     nsum = np.array([case.n_full_pages(b) for b in range(case.batch)])
     r = O.decode_step(case.q, case.k_pool, case.v_pool, case.block_table, case.seq_lens, nsum,
-                      basis, coeffs, case.num_kv_heads, budget_tokens=10 ** 6)
+                      basis, coeffs, case.num_kv_heads, budget_tokens=10 ** 6, page_size=P)
     od, ld = O.dense_decode(case.q, case.k_pool, case.v_pool, case.block_table, case.seq_lens,
-                            case.num_kv_heads)
+                            case.num_kv_heads, page_size=P)
     assert np.allclose(r["out"], od, atol=1e-12)
     assert np.allclose(r["lse"], ld, atol=1e-12)
     assert np.isfinite(r["out"]).all()  # NaN-poisoned slots past seq_len never read
 
 
-def test_sparse_equals_dense_over_chosen_tokens():
+@pytest.mark.parametrize("P", [64, 16])
+def test_sparse_equals_dense_over_chosen_tokens(P):
     """Attention over selected pages + tail equals attention over exactly those
     tokens gathered by hand; the open tail is always included."""
-    case = _small_case(seed=10)
+    case = _small_case(seed=10, P=P)
     basis, coeffs = _oracle_summaries(case, 8)
     nsum = np.array([case.n_full_pages(b) - 1 for b in range(case.batch)])  # last full page unsummarised
     r = O.decode_step(case.q, case.k_pool, case.v_pool, case.block_table, case.seq_lens, nsum,
-                      basis, coeffs, case.num_kv_heads, budget_tokens=64 * 5)
+                      basis, coeffs, case.num_kv_heads, budget_tokens=P * 5, page_size=P)
     kf, vf, qf = O.bf16_widen(case.k_pool), O.bf16_widen(case.v_pool), O.bf16_widen(case.q)
     G = case.group
     for (b, h), pages in r["sel"].items():
@@ -294,7 +298,7 @@ def test_sparse_equals_dense_over_chosen_tokens():
         allp = list(pages) + list(range(int(nsum[b]), case.n_pages(b)))
         for j in allp:
             p = case.block_table[b, j]
-            n = min(64, L - 64 * j)
+            n = min(P, L - P * j)
             toks_k.append(kf[p, h, :n])
             toks_v.append(vf[p, h, :n])
         o, l = O.attention(qf[b, h * G:(h + 1) * G], np.concatenate(toks_k), np.concatenate(toks_v))
