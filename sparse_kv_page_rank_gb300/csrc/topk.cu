@@ -208,16 +208,16 @@ __device__ void block_select(const uint32_t* keys, int n, int k, SelectShared& s
 // bits in which the keys differ (2048 bins) finds the bin that holds the
 // k-th largest key; keys in higher bins are all taken, and the few keys of
 // that boundary bin are ranked against each other (key descending, element
-// ascending) to take the rest.  The chosen elements are then numbered in
+// ascending; one 64-bit word per key, (key, ~element), compared with 16-byte
+// loads) to take the rest.  The chosen elements are then numbered in
 // element order with warp ballots.  When the boundary bin holds more than
 // kBoundaryMax keys (many equal or nearly equal keys) the radix select above
 // runs instead, on the same keys in shared memory (`keys_smem`).  Output
 // order and ties are as in block_select.
-constexpr int kBoundaryMax = 256;
+constexpr int kBoundaryMax = kTopkThreads;  // one boundary key per thread
 struct __align__(16) FastShared {
   unsigned bins[2048];
-  uint32_t bkey[kBoundaryMax];
-  int bidx[kBoundaryMax];
+  unsigned long long bcomb[kBoundaryMax];  // (key << 32) | ~element; zero past the bin's keys
   unsigned char bwin[kBoundaryMax];
   int wsum[kWarps];
   unsigned wmin[kWarps], wmax[kWarps];
@@ -253,6 +253,7 @@ __device__ void reg_select(const uint32_t (&kr)[IPT], const uint32_t* keys_smem,
     fs.wmax[warp] = hi;
   }
   reinterpret_cast<uint4*>(fs.bins)[tid] = make_uint4(0u, 0u, 0u, 0u);
+  fs.bcomb[tid] = 0ull;  // below every real key: padding of the ranking loop
   if (tid == 0) fs.b_cnt = 0;
   __syncthreads();
 #pragma unroll
@@ -320,19 +321,20 @@ __device__ void reg_select(const uint32_t (&kr)[IPT], const uint32_t* keys_smem,
       base = __shfl_sync(0xffffffffu, base, 0);
     }
     bslot[u] = eq ? base + __popc(mask & ((1u << lane) - 1u)) : -1;
-    if (eq) {
-      fs.bkey[bslot[u]] = kr[u];
-      fs.bidx[bslot[u]] = tid + kTopkThreads * u;
-    }
+    if (eq) fs.bcomb[bslot[u]] = ((unsigned long long)kr[u] << 32) | (0xffffffffu - (uint32_t)(tid + kTopkThreads * u));
   }
   __syncthreads();
   if (tid < (int)m) {
-    const uint32_t mk = fs.bkey[tid];
-    const int mi = fs.bidx[tid];
+    // rank = keys ahead of this one (larger key, or equal key and lower
+    // element); the zero padding up to a multiple of 8 is ahead of nothing
+    const unsigned long long mine = fs.bcomb[tid];
+    const ulonglong2* bc = reinterpret_cast<const ulonglong2*>(fs.bcomb);
+    const int m8 = ((int)m + 7) >> 3;
     int rank = 0;
-    for (int v = 0; v < (int)m; ++v) {
-      const uint32_t ok = fs.bkey[v];
-      rank += (ok > mk) || (ok == mk && fs.bidx[v] < mi);
+    for (int v = 0; v < m8; ++v) {
+      const ulonglong2 x0 = bc[4 * v], x1 = bc[4 * v + 1], x2 = bc[4 * v + 2], x3 = bc[4 * v + 3];
+      rank += (x0.x > mine) + (x0.y > mine) + (x1.x > mine) + (x1.y > mine) + (x2.x > mine) + (x2.y > mine) +
+              (x3.x > mine) + (x3.y > mine);
     }
     fs.bwin[tid] = rank < need ? 1 : 0;
   }

@@ -281,3 +281,51 @@ def test_p16_q4_builder_reconstruction(r):
             de = abs(O.reconstruction_error(K, Vg, Cg, mug) - O.reconstruction_error(K, Vo, Co, muo))
             worst = max(worst, de)
     assert worst <= 1e-3, worst
+
+
+def test_p16_graph_capture_replay_bit_identical():
+    case = make_case(2, 8, 2, [P * 133 + 7, P * 120], true_rank=(2, 10), seed=350, page_size=P)
+    basis_t, coeffs = oracle_summaries_bf16(case, 8)
+    rt, q = make_runtime(case, 8, budget_tokens=P * 14)
+    rt.set_summaries(to_torch_bf16(basis_t, rt.device), to_torch_bf16(coeffs, rt.device))
+    out_e, lse_e = rt.decode_step(q)
+    ref_o, ref_l, ref_sel = out_e.clone(), lse_e.clone(), rt.sel_pages.clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    out_g, lse_g = torch.zeros_like(out_e), torch.zeros_like(lse_e)
+    with torch.cuda.stream(s):
+        rt.decode_step(q, out_g, lse_g, stream=s)
+        with torch.cuda.graph(g, stream=s):
+            rt.decode_step(q, out_g, lse_g, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(3):
+        out_g.zero_()
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out_g, ref_o) and torch.equal(lse_g, ref_l) and torch.equal(rt.sel_pages, ref_sel)
+    # lengths are read on the device: shrink sequence 0's partial tail page
+    rt.seq_lens[0] -= 1
+    g.replay()
+    torch.cuda.synchronize()
+    assert not torch.equal(out_g[0], ref_o[0])
+    assert torch.equal(out_g[1], ref_o[1])
+    assert rt.device_error() == 0
+
+
+def test_p16_device_error_on_bad_block_table_and_length():
+    case = make_case(1, 4, 2, P * 10 + 5, seed=351, page_size=P)
+    basis_t, coeffs = oracle_summaries_bf16(case, 8)
+    rt, q = make_runtime(case, 8, budget_tokens=P * 3)
+    rt.set_summaries(to_torch_bf16(basis_t, rt.device), to_torch_bf16(coeffs, rt.device))
+    good = rt.block_table.clone()
+    rt.block_table[0, 2] = case.pages_total + 5   # out of range: skipped, flagged
+    rt.decode_step(q)
+    rt.dense_decode(q)
+    assert rt.device_error() & 0x1
+    rt.block_table.copy_(good)
+    rt.decode_step(q)
+    assert rt.device_error() == 0
+    rt.seq_lens[0] = P * case.max_pages + 1       # longer than max_pages * P
+    rt.decode_step(q)
+    assert rt.device_error() & 0x4
