@@ -47,17 +47,20 @@ FALLBACK_HBM_GBS = 6800.0
 P, D = 64, 128
 
 # DRAM traffic (bytes read + written) of one summary-scan launch per
-# summarised page-head, from ncu captures of the scan kernel on these
-# workloads (profiles/scan_kernel_llama128k.md, profiles/scan_kernel_ctx1m.md);
-# valid only while scan.cu is unchanged since those captures.
+# summarised page-head, keyed by (workload, page size), from ncu captures of
+# the scan kernel (profiles/scan_kernel_llama128k.md, scan_kernel_ctx1m.md,
+# scan_kernel_llama128k_page16.md); valid only while scan.cu is unchanged
+# since those captures.
 SCAN_TRAFFIC_PER_PAGE_HEAD = {
-    "llama128k": (50365952 + 31232) / 16384,
+    ("llama128k", 64): (50365952 + 2816) / 16384,
+    ("ctx1m", 64): (100761088 + 3253760) / 32768,
+    ("llama128k", 16): (151064832 + 3976448) / 65536,
 }
 # the same for the quantised summary format (profiles/scan_kernel_q4_llama128k.md)
 SCAN_Q4_TRAFFIC_PER_PAGE_HEAD = {
-    "llama128k": (20229632 + 0) / 16384,
+    ("llama128k", 64): (20229632 + 0) / 16384,
 }
-SCAN_TRAFFIC_SOURCE_SHA = "dffae15537cd5e27"
+SCAN_TRAFFIC_SOURCE_SHA = "8ef72a34c0a70c64"
 
 
 # ---------------------------------------------------------------------------
@@ -500,9 +503,8 @@ def run_gpu(args):
         qb = q4_page_head_bytes(r, P)
         q_scan_alg = Hkv * int(nsum_host.sum()) * (qb + G * 4)
         q_traffic = None
-        if args.config in SCAN_Q4_TRAFFIC_PER_PAGE_HEAD and SCAN_TRAFFIC_SOURCE_SHA == _scan_source_sha() \
-                and P == 64:
-            q_traffic = SCAN_Q4_TRAFFIC_PER_PAGE_HEAD[args.config] * Hkv * int(nsum_host.sum())
+        if (args.config, P) in SCAN_Q4_TRAFFIC_PER_PAGE_HEAD and SCAN_TRAFFIC_SOURCE_SHA == _scan_source_sha():
+            q_traffic = SCAN_Q4_TRAFFIC_PER_PAGE_HEAD[(args.config, P)] * Hkv * int(nsum_host.sum())
         q4 = {"value": q4_step_ms * 1e3, "unit": "us", "summary_bytes_per_page_head": qb,
               "residency": qb / (2 * P * D * 2), "speedup_vs_dense": dense_ms / q4_step_ms,
               "scan_us": q4_scan_ms * 1e3, "scan_gbs": q_scan_alg / (q4_scan_ms * 1e-3) / 1e9,
@@ -527,8 +529,8 @@ def run_gpu(args):
     scan_gbs = scan_alg / (scan_ms * 1e-3) / 1e9
     dense_gbs = db / (dense_ms * 1e-3) / 1e9
     traffic = None
-    if args.config in SCAN_TRAFFIC_PER_PAGE_HEAD and SCAN_TRAFFIC_SOURCE_SHA == _scan_source_sha() and P == 64:
-        traffic = SCAN_TRAFFIC_PER_PAGE_HEAD[args.config] * Hkv * n_sum_tot
+    if (args.config, P) in SCAN_TRAFFIC_PER_PAGE_HEAD and SCAN_TRAFFIC_SOURCE_SHA == _scan_source_sha():
+        traffic = SCAN_TRAFFIC_PER_PAGE_HEAD[(args.config, P)] * Hkv * n_sum_tot
 
     # CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only)
     cpu = None
