@@ -530,42 +530,59 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkArgs a)
   trace_mark(a.err, kTrTopkKeys, false);
 
   const int kloc = k < nloc ? k : nloc;
-  if (a.n_chunks == 1) {
-    reg_select<IPT>(kr, keys, nloc, kloc, sh, fsh, [&](int pos, int i) { sel[pos] = j0 + i; }, a.err);
-    if (tid == 0) a.sel_count[bh] = kloc;
-    trace_mark(a.err, kTrTopkSelected, false);
-    trace_mark(a.err, kTrTopkExit, false);
-    return;
-  }
-
   uint32_t* ck = a.cand_key + ((size_t)bh * a.n_chunks + chunk) * a.k_max;
   int32_t* ci = a.cand_idx + ((size_t)bh * a.n_chunks + chunk) * a.k_max;
-  reg_select<IPT>(kr, keys, nloc, kloc, sh, fsh, [&](int pos, int i) {
-    ck[pos] = keys[i];
-    ci[pos] = j0 + i;
-  });
-  // unused candidate slots get the lowest key (never chosen: the chunks
-  // together always offer at least k real candidates)
-  for (int j = kloc + tid; j < a.k_max; j += kTopkThreads) {
-    ck[j] = 0u;
-    ci[j] = -1;
-  }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    unsigned prev = atomicAdd(a.counters + bh, 1u);
-    is_last = prev == (unsigned)(a.n_chunks - 1);
-  }
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-
-  // every chunk's candidate slots, chunk-major (= page order), in one round trip
   const int n_all = a.n_chunks * a.k_max;
-  const uint32_t* gk = a.cand_key + (size_t)bh * n_all;
-  const int32_t* gi = a.cand_idx + (size_t)bh * n_all;
-  auto emit_merged = [&](int pos, int i) { sel[pos] = idx[i]; };
-  if (n_all <= IPT * kTopkThreads) {
+  // One call site of the selection.  Every CTA runs it once; with several
+  // chunks the last CTA of a problem runs it again over all chunks'
+  // candidates, re-executing instructions it has just fetched rather than a
+  // second inlined copy that no SM has run yet (cold instruction fetch made
+  // that copy about three times slower than the work it does).
+  // mode 0: one chunk, straight to the page list; 1: this chunk's candidates;
+  // 2: the merge (element i = candidate slot i, page idx[i]).
+  int mode = a.n_chunks == 1 ? 0 : 1;
+  int sn = nloc, sk = kloc;
+#pragma unroll 1
+  for (;;) {
+    reg_select<IPT>(kr, keys, sn, sk, sh, fsh, [&](int pos, int i) {
+      if (mode == 0) {
+        sel[pos] = j0 + i;
+      } else if (mode == 1) {
+        ck[pos] = keys[i];
+        ci[pos] = j0 + i;
+      } else {
+        sel[pos] = idx[i];
+      }
+    }, mode == 0 ? a.err : nullptr);
+    if (mode != 1) break;
+    // unused candidate slots get the lowest key (never chosen: the chunks
+    // together always offer at least k real candidates)
+    for (int j = kloc + tid; j < a.k_max; j += kTopkThreads) {
+      ck[j] = 0u;
+      ci[j] = -1;
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+      unsigned prev = atomicAdd(a.counters + bh, 1u);
+      is_last = prev == (unsigned)(a.n_chunks - 1);
+    }
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    // every chunk's candidate slots, chunk-major (= page order), in one round trip
+    const uint32_t* gk = a.cand_key + (size_t)bh * n_all;
+    const int32_t* gi = a.cand_idx + (size_t)bh * n_all;
+    if (n_all > IPT * kTopkThreads) {
+      // more candidates than registers hold: radix select in shared memory
+      for (int i = tid; i < n_all; i += kTopkThreads) {
+        keys[i] = __ldcg(gk + i);
+        idx[i] = __ldcg(gi + i);
+      }
+      __syncthreads();
+      block_select(keys, n_all, k, sh, [&](int pos, int i) { sel[pos] = idx[i]; });
+      break;
+    }
 #pragma unroll
     for (int u = 0; u < IPT; ++u) {
       const int i = tid + kTopkThreads * u;
@@ -576,19 +593,15 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkArgs a)
         idx[i] = __ldcg(gi + i);
       }
     }
-    reg_select<IPT>(kr, keys, n_all, k, sh, fsh, emit_merged);
-  } else {
-    for (int i = tid; i < n_all; i += kTopkThreads) {
-      keys[i] = __ldcg(gk + i);
-      idx[i] = __ldcg(gi + i);
-    }
-    __syncthreads();
-    block_select(keys, n_all, k, sh, emit_merged);
+    sn = n_all;
+    sk = k;
+    mode = 2;
   }
   if (tid == 0) {
-    a.sel_count[bh] = k;
-    a.counters[bh] = 0;  // ready for the next call
+    a.sel_count[bh] = a.n_chunks == 1 ? kloc : k;
+    if (a.n_chunks > 1) a.counters[bh] = 0;  // ready for the next call
   }
+  if (a.n_chunks == 1) trace_mark(a.err, kTrTopkSelected, false);
   trace_mark(a.err, kTrTopkExit, false);
 }
 
