@@ -392,9 +392,11 @@ __device__ void reg_select(const uint32_t (&kr)[IPT], const uint32_t* keys_smem,
 }
 
 // GT: heads per group (compile time; 0 = any G <= 16 at run time).
+// MULTI: several chunks per problem (candidates, then a merge by the last
+// CTA); a problem of one chunk selects straight into the page list.
 // Each thread owns IPT consecutive pages of the chunk, whose s_hat rows it
 // loads together with the lengths and the scan partials in one round trip.
-template <int GT>
+template <int GT, bool MULTI>
 __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkArgs a) {
   constexpr int GMAX = GT ? GT : 16;
   constexpr int IPT = GT ? (32 / GT < 8 ? 32 / GT : 8) : 2;  // pages per thread
@@ -530,30 +532,35 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkArgs a)
   trace_mark(a.err, kTrTopkKeys, false);
 
   const int kloc = k < nloc ? k : nloc;
+  if constexpr (!MULTI) {
+    reg_select<IPT>(kr, keys, nloc, kloc, sh, fsh, [&](int pos, int i) { sel[pos] = j0 + i; }, a.err);
+    if (tid == 0) a.sel_count[bh] = kloc;
+    trace_mark(a.err, kTrTopkSelected, false);
+    trace_mark(a.err, kTrTopkExit, false);
+    return;
+  }
   uint32_t* ck = a.cand_key + ((size_t)bh * a.n_chunks + chunk) * a.k_max;
   int32_t* ci = a.cand_idx + ((size_t)bh * a.n_chunks + chunk) * a.k_max;
   const int n_all = a.n_chunks * a.k_max;
-  // One call site of the selection.  Every CTA runs it once; with several
-  // chunks the last CTA of a problem runs it again over all chunks'
-  // candidates, re-executing instructions it has just fetched rather than a
-  // second inlined copy that no SM has run yet (cold instruction fetch made
-  // that copy about three times slower than the work it does).
-  // mode 0: one chunk, straight to the page list; 1: this chunk's candidates;
-  // 2: the merge (element i = candidate slot i, page idx[i]).
-  int mode = a.n_chunks == 1 ? 0 : 1;
+  // One call site of the selection.  Every CTA runs it once over its chunk;
+  // the last CTA of a problem runs it again over all chunks' candidates,
+  // re-executing instructions it has just fetched rather than a second
+  // inlined copy that no SM has run yet (cold instruction fetch made that
+  // copy about three times slower than the work it does).
+  // mode 1: this chunk's candidates; 2: the merge (element i = candidate
+  // slot i, page idx[i]).
+  int mode = 1;
   int sn = nloc, sk = kloc;
 #pragma unroll 1
   for (;;) {
     reg_select<IPT>(kr, keys, sn, sk, sh, fsh, [&](int pos, int i) {
-      if (mode == 0) {
-        sel[pos] = j0 + i;
-      } else if (mode == 1) {
+      if (mode == 1) {
         ck[pos] = keys[i];
         ci[pos] = j0 + i;
       } else {
         sel[pos] = idx[i];
       }
-    }, mode == 0 ? a.err : nullptr);
+    });
     if (mode != 1) break;
     // unused candidate slots get the lowest key (never chosen: the chunks
     // together always offer at least k real candidates)
@@ -598,10 +605,9 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkArgs a)
     mode = 2;
   }
   if (tid == 0) {
-    a.sel_count[bh] = a.n_chunks == 1 ? kloc : k;
-    if (a.n_chunks > 1) a.counters[bh] = 0;  // ready for the next call
+    a.sel_count[bh] = k;
+    a.counters[bh] = 0;  // ready for the next call
   }
-  if (a.n_chunks == 1) trace_mark(a.err, kTrTopkSelected, false);
   trace_mark(a.err, kTrTopkExit, false);
 }
 
@@ -612,10 +618,11 @@ size_t topk_smem_bytes(size_t keys) { return keys * (sizeof(uint32_t) + sizeof(i
 
 namespace {
 
-template <int GT>
-cudaError_t launch_g(const TopkArgs& a, cudaStream_t s, bool pdl) {
+template <int GT, bool MULTI>
+cudaError_t launch_gm(const TopkArgs& a, cudaStream_t s, bool pdl) {
   const size_t smem = topk_smem_bytes(a.smem_keys);
-  cudaError_t e = cudaFuncSetAttribute(topk_kernel<GT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e =
+      cudaFuncSetAttribute(topk_kernel<GT, MULTI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_chunks, a.batch * a.num_kv_heads, 1);
@@ -627,7 +634,12 @@ cudaError_t launch_g(const TopkArgs& a, cudaStream_t s, bool pdl) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, topk_kernel<GT>, a);
+  return cudaLaunchKernelEx(&cfg, topk_kernel<GT, MULTI>, a);
+}
+
+template <int GT>
+cudaError_t launch_g(const TopkArgs& a, cudaStream_t s, bool pdl) {
+  return a.n_chunks > 1 ? launch_gm<GT, true>(a, s, pdl) : launch_gm<GT, false>(a, s, pdl);
 }
 
 }  // namespace
