@@ -18,7 +18,7 @@ Notation follows the pages: a page j holds P tokens with keys k_i (i in P_j),
 its summary is a basis V_j (d x r) and coefficients c_i (r-vectors, stacked into
 C_j, P x r), optionally a centroid mu_j; d is the head dimension.
 
-Readings where the pages are silent (each one is listed in the design doc):
+Readings where the pages are silent:
   * the summary is the rank-r truncated SVD of the raw P x d key block
     (V_r = right singular vectors, C = U_r Sigma_r); the centred variant of the
     explainer subtracts the page mean first and adds the q.mu_j term;
