@@ -35,7 +35,7 @@
  *    stream (except locks_get_device_error, which reads back one word).
  *  - Element types: keys, values, queries, outputs and summaries are bf16
  *    (raw 16-bit patterns), lengths and indices int32, scores float32.
- *  - Sizes in this build: head_dim d = 128, page_size P = 64 or 16 (the
+ *  - Supported sizes: head_dim d = 128, page_size P = 64 or 16 (the
  *    explainer's §2 "Kernmechanisme" gives a page size of 16), group size
  *    G = num_q_heads / num_kv_heads in 1..16, summary rank r even in 2..16
  *    (and r <= P).  Other values return LOCKS_ERR_UNSUPPORTED.
@@ -71,7 +71,7 @@ extern "C" {
 typedef enum {
   LOCKS_OK = 0,
   LOCKS_ERR_INVALID_ARG = 1,   /* null pointer, negative size, inconsistent shapes */
-  LOCKS_ERR_UNSUPPORTED = 2,   /* a size this build does not implement (d, P, G, r) */
+  LOCKS_ERR_UNSUPPORTED = 2,   /* a size the library does not implement (d, P, G, r) */
   LOCKS_ERR_CUDA = 3,          /* a CUDA runtime call or kernel launch failed */
   LOCKS_ERR_WORKSPACE = 4,     /* workspace missing, too small or misaligned */
   LOCKS_ERR_DEVICE = 5         /* returned by locks_get_device_error when a bit is set */
