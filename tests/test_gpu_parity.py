@@ -124,6 +124,39 @@ def test_many_chunks_scan_and_topk(G, pages):
     _run_case(case, 8, budget=64 * 40, check_dense=True)
 
 
+def test_merge_of_more_candidates_than_registers_hold():
+    """Three top-k chunks (G = 16: 1024 pages each) offering 400 candidates
+    each: the 1200 candidates exceed the merge's register capacity (1024), so
+    the last CTA merges them with the radix select in shared memory."""
+    case = make_case(1, 16, 1, 64 * 3000 + 3, true_rank=(4, 12), n_carriers=16, seed=21)
+    _run_case(case, 8, budget=64 * 400, check_dense=False)
+
+
+def test_boundary_bin_of_many_equal_keys():
+    """1500 logical pages share one physical page (the planted carrier), so
+    their scores are bit-identical and larger than every other page's; with
+    k = 600 the boundary bin holds 1500 keys, more than the histogram select
+    ranks itself, and the radix select takes over.  Ties go to the lower
+    page, so exactly logical pages 0..599 are chosen."""
+    case = make_case(1, 1, 1, 64 * 2000, true_rank=(2, 8), n_carriers=1, seed=77)
+    c = int(case.carriers[0, 0, 0])
+    case.block_table[0, :1500] = case.block_table[0, c]
+    nsum = [case.n_full_pages(0)]
+    pages = sorted(set(int(x) for x in case.block_table[0, :nsum[0]]))
+    basis_t, coeffs = oracle_summaries_bf16(case, 8, pages=pages)
+    rt, q = make_runtime(case, 8, 64 * 600, nsum)
+    _upload_summaries(rt, basis_t, coeffs)
+    rt.select(q)
+    torch.cuda.synchronize()
+    assert rt.device_error() == 0
+    ob, oc = oracle_layout_from_abi(basis_t, coeffs)
+    ref = O.decode_step(case.q, case.k_pool, case.v_pool, case.block_table, case.seq_lens, nsum, ob, oc,
+                        case.num_kv_heads, 64 * 600)
+    assert list(ref["sel"][(0, 0)]) == list(range(600))  # the oracle's own tie rule
+    assert int(rt.sel_count[0, 0]) == 600
+    assert rt.sel_pages[0, 0, :600].cpu().tolist() == list(range(600))
+
+
 def test_tiny_workload_carrier_kept():
     case, cfg = make_config_case("tiny")
     rt, q, ref, _ = _run_case(case, cfg["rank"], cfg["budget_tokens"])
