@@ -2,6 +2,7 @@
 one pin in test_oracle_pins.py fails for each: evidence that the pins would
 catch a dropped term, a wrong sign or index, or a transposed operand."""
 
+import functools
 import math
 
 import numpy as np
@@ -91,7 +92,11 @@ def _quant_wide_scale(x, qmax):
     return ORIG["quantize_symmetric"](x, qmax + 1)
 
 
-ORIG = {n: getattr(L, n) for n in ("page_summary", "attention", "quantize_symmetric")}
+def _page_tokens_fixed_64(pool_f64, block_table, b, h, pages, seq_len, P):
+    return ORIG["_page_tokens"](pool_f64, block_table, b, h, pages, seq_len, 64)
+
+
+ORIG = {n: getattr(L, n) for n in ("page_summary", "attention", "quantize_symmetric", "_page_tokens")}
 
 MUTANTS = {
     "lse_without_max_shift": ("logsumexp", _lse_no_shift),
@@ -105,7 +110,15 @@ MUTANTS = {
     "attention_without_scale": ("attention", _attention_no_scale),
     "quantize_truncates": ("quantize_symmetric", _quant_floor),
     "quantize_scale_one_code_too_wide": ("quantize_symmetric", _quant_wide_scale),
+    "page_tokens_assume_64_token_pages": ("_page_tokens", _page_tokens_fixed_64),
 }
+
+
+def _at_page_size(test, P):
+    f = functools.partial(test, P=P)
+    f.__name__ = f"{test.__name__}[P={P}]"
+    return f
+
 
 PIN_TESTS = [
     pins.test_lse_brute_force_tiny_pages,
@@ -121,6 +134,8 @@ PIN_TESTS = [
     pins.test_quantize_roundtrip_within_half_step,
     pins.test_quantize_exact_on_its_grid,
     pins.test_quantized_summary_dequantizes_to_the_summary,
+    _at_page_size(pins.test_sparse_equals_dense_over_chosen_tokens, 64),
+    _at_page_size(pins.test_sparse_equals_dense_over_chosen_tokens, 16),
 ]
 
 
@@ -128,7 +143,8 @@ PIN_TESTS = [
 def test_pins_catch_mutant(name, monkeypatch):
     attr, fn = MUTANTS[name]
     monkeypatch.setattr(L, attr, fn)
-    monkeypatch.setattr(oracle, attr, fn)
+    if hasattr(oracle, attr):
+        monkeypatch.setattr(oracle, attr, fn)
     failed = []
     for t in PIN_TESTS:
         try:
