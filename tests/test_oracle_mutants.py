@@ -96,7 +96,44 @@ def _page_tokens_fixed_64(pool_f64, block_table, b, h, pages, seq_len, P):
     return ORIG["_page_tokens"](pool_f64, block_table, b, h, pages, seq_len, 64)
 
 
-ORIG = {n: getattr(L, n) for n in ("page_summary", "attention", "quantize_symmetric", "_page_tokens")}
+def _recon_error_over_reconstruction_norm(K, V, C, mu=None):
+    K = np.asarray(K, dtype=np.float64)
+    R = C @ V.T
+    if mu is not None:
+        R = R + np.asarray(mu, dtype=np.float64)[None, :]
+    nr = np.linalg.norm(R)
+    return float(np.linalg.norm(K - R) / nr) if nr > 0 else 1.0
+
+
+def _recon_error_without_centroid(K, V, C, mu=None):
+    return ORIG["reconstruction_error"](K, V, C, None)
+
+
+def _sparse_decode_variant(drop_tail=False, floor_pages=False):
+    def f(q, k_pool, v_pool, block_table, seq_lens, n_summarized, sel, num_kv_heads, page_size=64, scale=None):
+        qf, kf, vf = L._widen(q), L._widen(k_pool), L._widen(v_pool)
+        B, Hq, d = qf.shape
+        G = Hq // num_kv_heads
+        P = page_size
+        out = np.zeros((B, Hq, d))
+        lse = np.full((B, Hq), -np.inf)
+        for b in range(B):
+            n = int(seq_lens[b])
+            n_pages = n // P if floor_pages else -(-n // P)
+            n_sum = min(int(n_summarized[b]), n // P)
+            for h in range(num_kv_heads):
+                pages = [int(j) for j in sel[(b, h)]] + ([] if drop_tail else list(range(n_sum, n_pages)))
+                Kt = L._page_tokens(kf, block_table, b, h, pages, n, P)
+                Vt = L._page_tokens(vf, block_table, b, h, pages, n, P)
+                o, l = L.attention(qf[b, h * G:(h + 1) * G], Kt, Vt, scale)
+                out[b, h * G:(h + 1) * G] = o
+                lse[b, h * G:(h + 1) * G] = l
+        return out, lse
+    return f
+
+
+ORIG = {n: getattr(L, n) for n in ("page_summary", "attention", "quantize_symmetric", "_page_tokens",
+                                   "reconstruction_error")}
 
 MUTANTS = {
     "lse_without_max_shift": ("logsumexp", _lse_no_shift),
@@ -111,6 +148,10 @@ MUTANTS = {
     "quantize_truncates": ("quantize_symmetric", _quant_floor),
     "quantize_scale_one_code_too_wide": ("quantize_symmetric", _quant_wide_scale),
     "page_tokens_assume_64_token_pages": ("_page_tokens", _page_tokens_fixed_64),
+    "reconstruction_error_over_reconstruction_norm": ("reconstruction_error", _recon_error_over_reconstruction_norm),
+    "reconstruction_error_ignores_centroid": ("reconstruction_error", _recon_error_without_centroid),
+    "sparse_decode_drops_the_tail": ("sparse_decode", _sparse_decode_variant(drop_tail=True)),
+    "sparse_decode_floor_page_count": ("sparse_decode", _sparse_decode_variant(floor_pages=True)),
 }
 
 
@@ -136,6 +177,11 @@ PIN_TESTS = [
     pins.test_quantized_summary_dequantizes_to_the_summary,
     _at_page_size(pins.test_sparse_equals_dense_over_chosen_tokens, 64),
     _at_page_size(pins.test_sparse_equals_dense_over_chosen_tokens, 16),
+    pins.test_reconstruction_error_closed_forms,
+    pins.test_reconstruction_error_equals_spectral_tail,
+    _at_page_size(pins.test_sparse_decode_equals_attention_over_listed_tokens, 64),
+    _at_page_size(pins.test_sparse_decode_every_page_equals_dense, 16),
+    pins.test_sparse_decode_on_decode_step_selection_equals_decode_step,
 ]
 
 

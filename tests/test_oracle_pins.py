@@ -413,3 +413,131 @@ def test_quantized_summary_dequantizes_to_the_summary():
     q = rng.standard_normal(128)
     direct = math.log(math.fsum(math.exp(v) for v in (C2 @ V2.T @ q + q @ mu2) / math.sqrt(128)))
     assert abs(O.reconstructed_page_lse(q, V2, C2, mu2) - direct) < 1e-12
+
+
+# --- reconstruction error (the builder's parity measure) ----------------------
+
+def test_reconstruction_error_closed_forms():
+    """Relative reconstruction error ||K - (1 mu^T + C V^T)||_F / ||K||_F, the
+    measure by which a summary is compared with the truncated SVD (explainer
+    §2 'Kernmechanisme'; Theorem 1, explainer §3, bounds the output error by
+    this residual).  Hand-built cases, no SVD involved:
+      * K has entries 3 at (0, 0) and 4 at (1, 1); the summary keeps the first
+        (V = e_0, C = 3 e_0): residual 4, ||K|| = 5, error 4/5 (dividing by
+        the reconstruction's norm 3 would give 4/3);
+      * a summary of all zeros reconstructs nothing: error 1;
+      * K = 1 mu^T + c v^T exactly, with mu given: error 0; the same summary
+        without mu leaves the centroid part: error ||1 mu^T|| / ||K||."""
+    P, d = 16, 32
+    K = np.zeros((P, d))
+    K[0, 0], K[1, 1] = 3.0, 4.0
+    V = np.zeros((d, 1))
+    V[0, 0] = 1.0
+    C = np.zeros((P, 1))
+    C[0, 0] = 3.0
+    assert abs(O.reconstruction_error(K, V, C) - 0.8) < 1e-15
+    assert O.reconstruction_error(K, np.zeros((d, 2)), np.zeros((P, 2))) == 1.0
+    rng = np.random.default_rng(21)
+    mu = rng.standard_normal(d)
+    v = _orth(rng, d, 1)
+    c = rng.standard_normal((P, 1))
+    K2 = np.tile(mu, (P, 1)) + c @ v.T
+    assert O.reconstruction_error(K2, v, c, mu) < 1e-14
+    want = math.sqrt(P) * np.linalg.norm(mu) / np.linalg.norm(K2)
+    assert abs(O.reconstruction_error(K2, v, c) - want) < 1e-12
+
+
+def test_reconstruction_error_equals_spectral_tail():
+    """For the rank-r truncated SVD the error is sqrt(sum_{i>r} sigma_i^2 /
+    sum_i sigma_i^2) (Eckart-Young): a page of exact rank 2 with singular
+    values (5, 2) has error 2/sqrt(29) at r = 1 and 0 at r = 2; a centred page
+    of identical keys has error 0 at any rank."""
+    rng = np.random.default_rng(22)
+    P, d = 16, 32
+    U = _orth(rng, P, 2)
+    W = _orth(rng, d, 2)
+    K = 5.0 * np.outer(U[:, 0], W[:, 0]) + 2.0 * np.outer(U[:, 1], W[:, 1])
+    V1, C1, _, _ = O.page_summary(K, 1)
+    assert abs(O.reconstruction_error(K, V1, C1) - 2.0 / math.sqrt(29.0)) < 1e-12
+    V2, C2, _, _ = O.page_summary(K, 2)
+    assert O.reconstruction_error(K, V2, C2) < 1e-13
+    k = rng.standard_normal(d)
+    Ki = np.tile(k, (P, 1))
+    Vc, Cc, muc, _ = O.page_summary(Ki, 3, centered=True)
+    assert O.reconstruction_error(Ki, Vc, Cc, muc) < 1e-14
+
+
+# --- sparse decode over a given page list --------------------------------------
+
+def _gather_by_token(pool_f64, block_table, b, h, pages, L, P):
+    """Rows of the listed logical pages' tokens, one token at a time: token t
+    of the sequence lives in physical page block_table[b, t // P], slot t % P,
+    and exists only for t < L."""
+    rows = []
+    for j in pages:
+        for t in range(j * P, (j + 1) * P):
+            if t < L:
+                rows.append(pool_f64[int(block_table[b, t // P]), h, t % P])
+    return np.array(rows).reshape(-1, pool_f64.shape[-1])
+
+
+@pytest.mark.parametrize("P", [64, 16])
+def test_sparse_decode_equals_attention_over_listed_tokens(P):
+    """Attention over the selected pages plus the open tail (LOCKS abstract:
+    only the top pages are attended; the open tail is read densely): for a
+    hand-chosen page list, with the last full page left unsummarised and a
+    partial last page, sparse_decode equals attention over exactly the tokens
+    of those pages and of every page from n_summarized to ceil(L / P) - 1,
+    gathered token by token."""
+    case = _small_case(seed=14, P=P)
+    nsum = np.array([case.n_full_pages(b) - 1 for b in range(case.batch)])
+    rng = np.random.default_rng(23)
+    sel = {(b, h): np.sort(rng.choice(int(nsum[b]), 4, replace=False))
+           for b in range(case.batch) for h in range(case.num_kv_heads)}
+    out, lse = O.sparse_decode(case.q, case.k_pool, case.v_pool, case.block_table, case.seq_lens, nsum, sel,
+                               case.num_kv_heads, page_size=P)
+    kf, vf, qf = O.bf16_widen(case.k_pool), O.bf16_widen(case.v_pool), O.bf16_widen(case.q)
+    G = case.group
+    for (b, h), pages in sel.items():
+        L = int(case.seq_lens[b])
+        assert L % P, "the case must end in a partial page"
+        tail = list(range(int(nsum[b]), -(-L // P)))
+        assert len(tail) == 2
+        Kt = _gather_by_token(kf, case.block_table, b, h, list(pages) + tail, L, P)
+        Vt = _gather_by_token(vf, case.block_table, b, h, list(pages) + tail, L, P)
+        assert Kt.shape[0] == 4 * P + P + L % P
+        o, l = O.attention(qf[b, h * G:(h + 1) * G], Kt, Vt)
+        assert np.allclose(out[b, h * G:(h + 1) * G], o, atol=1e-12)
+        assert np.allclose(lse[b, h * G:(h + 1) * G], l, atol=1e-12)
+
+
+@pytest.mark.parametrize("P", [64, 16])
+def test_sparse_decode_every_page_equals_dense(P):
+    """Listing every summarised page leaves nothing out: with the tail added
+    the token set is the whole sequence, so sparse_decode equals dense
+    attention (and an empty list with nothing summarised does too)."""
+    case = _small_case(seed=15, P=P)
+    nsum = np.array([case.n_full_pages(b) - 2 for b in range(case.batch)])
+    allsel = {(b, h): np.arange(int(nsum[b])) for b in range(case.batch) for h in range(case.num_kv_heads)}
+    out, lse = O.sparse_decode(case.q, case.k_pool, case.v_pool, case.block_table, case.seq_lens, nsum, allsel,
+                               case.num_kv_heads, page_size=P)
+    od, ld = O.dense_decode(case.q, case.k_pool, case.v_pool, case.block_table, case.seq_lens,
+                            case.num_kv_heads, page_size=P)
+    assert np.allclose(out, od, atol=1e-12) and np.allclose(lse, ld, atol=1e-12)
+    none = {k: np.zeros(0, int) for k in allsel}
+    out0, lse0 = O.sparse_decode(case.q, case.k_pool, case.v_pool, case.block_table, case.seq_lens,
+                                 np.zeros(case.batch, int), none, case.num_kv_heads, page_size=P)
+    assert np.allclose(out0, od, atol=1e-12) and np.allclose(lse0, ld, atol=1e-12)
+
+
+def test_sparse_decode_on_decode_step_selection_equals_decode_step():
+    """sparse_decode on the page lists that decode_step selected gives
+    decode_step's own output: the two restate one page-list rule."""
+    case = _small_case(seed=16)
+    basis, coeffs = _oracle_summaries(case, 4)
+    nsum = np.array([case.n_full_pages(b) - 1 for b in range(case.batch)])
+    r = O.decode_step(case.q, case.k_pool, case.v_pool, case.block_table, case.seq_lens, nsum,
+                      basis, coeffs, case.num_kv_heads, budget_tokens=64 * 6)
+    out, lse = O.sparse_decode(case.q, case.k_pool, case.v_pool, case.block_table, case.seq_lens, nsum,
+                               r["sel"], case.num_kv_heads)
+    assert np.allclose(out, r["out"], atol=1e-13) and np.allclose(lse, r["lse"], atol=1e-13)
