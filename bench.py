@@ -48,15 +48,14 @@ P, D = 64, 128
 
 # DRAM traffic (bytes read + written) of one summary-scan launch per
 # summarised page-head, keyed by (workload, page size), from ncu captures of
-# the scan kernel (profiles/scan_kernel_llama128k.md, scan_kernel_ctx1m.md,
-# scan_kernel_llama128k_page16.md); valid only while scan.cu is unchanged
+# the scan kernel at each workload; valid only while scan.cu is unchanged
 # since those captures.
 SCAN_TRAFFIC_PER_PAGE_HEAD = {
     ("llama128k", 64): (50365952 + 2816) / 16384,
     ("ctx1m", 64): (100761088 + 3253760) / 32768,
     ("llama128k", 16): (151064832 + 3976448) / 65536,
 }
-# the same for the quantised summary format (profiles/scan_kernel_q4_llama128k.md)
+# the same for the quantised summary format
 SCAN_Q4_TRAFFIC_PER_PAGE_HEAD = {
     ("llama128k", 64): (20229632 + 0) / 16384,
 }
