@@ -571,7 +571,7 @@ def run_gpu(args):
                 "memcpy_how": "the same with cudaMemcpyAsync of q (pinned host -> device) before and of out "
                               "(device -> pinned host) after each step"},
         "q4": q4,
-        "gpu_launches": 3 * K,
+        "gpu_launches": rts[0].decode_step_launches() * K,
         "clocks": clk,
     }
     if rank == 0:

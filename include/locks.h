@@ -159,8 +159,15 @@ typedef struct locks_params {
   int32_t num_q_heads;
   int32_t budget_tokens;
   float scale;     /* 0 -> 1/sqrt(head_dim) */
-  int32_t flags;   /* reserved, must be 0 */
+  int32_t flags;   /* 0 or LOCKS_FLAG_UNFUSED; other bits are reserved and must be 0 */
 } locks_params_t;
+
+/* locks_decode_step normally runs as two kernels when page_size is 64, k_max
+ * <= 32 and max_pages <= 128 x (the largest thread-block cluster, 16 CTAs):
+ * the summary scan, then one attention kernel whose clusters compute the
+ * group-shared top-k themselves.  This flag makes it run the three-kernel
+ * form (scan, top-k, attention) instead; both select the same pages. */
+#define LOCKS_FLAG_UNFUSED 0x1
 
 /* Human-readable name of a status code (static string). */
 LOCKS_API const char* locks_status_string(locks_status_t status);
@@ -232,12 +239,24 @@ LOCKS_API locks_status_t locks_sparse_attend(const locks_cache_t* cache, const l
 
 /* locks_select followed by locks_sparse_attend in one call (no host work
  * between the launches, programmatic dependent launch between kernels).
- * sel_pages / sel_count may be NULL (then kept in the workspace).  This is
- * the whole decode step; capture it in a CUDA graph for replay. */
+ * sel_pages / sel_count may be NULL (then kept in the workspace); when given
+ * they receive the page list as locks_select writes it.  This is the whole
+ * decode step; capture it in a CUDA graph for replay.  Where the shapes allow
+ * (see LOCKS_FLAG_UNFUSED) the top-k runs inside the attention kernel: each
+ * sequence's thread-block cluster scores its pages, exchanges its best
+ * candidates through distributed shared memory and attends to the pages it
+ * selected, and the K/V of the open tail is loaded while the scan is still
+ * running. */
 LOCKS_API locks_status_t locks_decode_step(const locks_cache_t* cache, const locks_summary_t* summary,
                                  const locks_params_t* params, const void* q, void* out,
                                  float* lse, int32_t* sel_pages, int32_t* sel_count,
                                  void* ws, size_t ws_bytes, void* stream);
+
+/* Number of kernels one locks_decode_step launches for these shapes: 2 (the
+ * scan, then attention with the top-k inside its clusters) or 3 (scan, top-k,
+ * attention); see LOCKS_FLAG_UNFUSED.  Host only; launches nothing. */
+LOCKS_API locks_status_t locks_decode_step_launches(const locks_cache_t* cache, const locks_summary_t* summary,
+                                                    const locks_params_t* params, int32_t* launches);
 
 /* Dense paged decode over every token of every sequence (the in-library
  * baseline the sparse step is measured against).  Same outputs as

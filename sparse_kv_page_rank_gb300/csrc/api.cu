@@ -37,6 +37,8 @@ struct Plan {
   int tk_chunk = 0, n_tk = 0;
   size_t tk_keys = 0;
   int sparse_cluster = 1, dense_cluster = 1, dense_nc = 1, lse_splits = 1;
+  bool fused = false;     // decode step as scan + one attention kernel that selects the pages itself
+  int fused_cluster = 1;
   size_t off_err = 0, off_cnt_tk = 0, off_cnt_att = 0, off_shat = 0, off_part = 0, off_ckey = 0,
          off_cidx = 0, off_sel = 0, off_selcnt = 0, off_pml = 0, off_po = 0, total = 0;
 };
@@ -63,7 +65,7 @@ locks_status_t check_params(const locks_cache_t* c, const locks_params_t* p) {
   if (p->num_q_heads <= 0 || p->num_q_heads % c->num_kv_heads) return LOCKS_ERR_INVALID_ARG;
   const int G = p->num_q_heads / c->num_kv_heads;
   if (G > 16) return LOCKS_ERR_UNSUPPORTED;
-  if (p->budget_tokens < 0 || p->flags != 0) return LOCKS_ERR_INVALID_ARG;
+  if (p->budget_tokens < 0 || (p->flags & ~LOCKS_FLAG_UNFUSED) != 0) return LOCKS_ERR_INVALID_ARG;
   if (!(p->scale >= 0.f) || !std::isfinite(p->scale)) return LOCKS_ERR_INVALID_ARG;
   return LOCKS_OK;
 }
@@ -154,6 +156,21 @@ Plan make_plan(const locks_cache_t* c, const locks_params_t* p) {
     }
     long long ls = (target + BH - 1) / BH;
     pl.lse_splits = (int)std::max<long long>(1, std::min<long long>(ls, max_tiles));
+    // fused step (64-token pages, k <= kFusedMaxK): one cluster per problem
+    // whose CTAs score at most one page per thread; sized like the sparse
+    // cluster, then raised until the pages fit
+    if (P == kPage && pl.k_max <= kFusedMaxK && !(p->flags & LOCKS_FLAG_UNFUSED)) {
+      const int cs_max = attend_max_cluster(kAttendFused, P);
+      const long long need = ((long long)c->max_pages + kAttendThreads - 1) / kAttendThreads;
+      int csf = 1;
+      while (csf * 2 <= cs_max && csf * 2 <= items) csf *= 2;
+      while (csf > 1 && BH > attend_active_clusters(kAttendFused, csf, P)) csf /= 2;
+      while (csf < need && csf * 2 <= cs_max) csf *= 2;
+      if (csf >= need) {
+        pl.fused = true;
+        pl.fused_cluster = csf;
+      }
+    }
   }
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -277,7 +294,7 @@ locks_status_t run_select(const locks_cache_t* c, const locks_summary_t* s, cons
 }
 
 locks_status_t run_attend(const locks_cache_t* c, const locks_params_t* p, const Plan& pl, const void* q,
-                          const int32_t* sel, const int32_t* selcnt, void* out, float* lse, float* page_lse,
+                          int32_t* sel, int32_t* selcnt, void* out, float* lse, float* page_lse,
                           void* ws, int mode, cudaStream_t st, bool inputs_early = false) {
   CUtensorMap tk, tv;
   std::memset(&tk, 0, sizeof(tk));
@@ -304,9 +321,23 @@ locks_status_t run_attend(const locks_cache_t* c, const locks_params_t* p, const
   a.max_pages = c->max_pages;
   a.pages_total = c->pages_total;
   a.k_max = pl.k_max;
+  a.shat = nullptr;
+  a.part = nullptr;
+  a.n_scan_chunks = pl.n_scan;
+  a.sel_pages_out = nullptr;
+  a.sel_count_out = nullptr;
   if (mode == kAttendSparse) {
     a.cluster = pl.sparse_cluster;
     a.n_splits = pl.sparse_cluster;
+  } else if (mode == kAttendFused) {
+    a.cluster = pl.fused_cluster;
+    a.n_splits = pl.fused_cluster;
+    a.shat = at<float>(ws, pl.off_shat);
+    a.part = at<float2>(ws, pl.off_part);
+    a.sel_pages_out = sel;
+    a.sel_count_out = selcnt;
+    a.sel_pages = nullptr;
+    a.sel_count = nullptr;
   } else if (mode == kAttendDense) {
     a.cluster = pl.dense_cluster;
     a.n_splits = pl.dense_cluster * pl.dense_nc;
@@ -423,8 +454,9 @@ locks_status_t locks_sparse_attend(const locks_cache_t* cache, const locks_param
   Plan pl = make_plan(cache, params);
   if (!pl.ok) return LOCKS_ERR_UNSUPPORTED;
   if ((st = check_ws(ws, ws_bytes, pl)) != LOCKS_OK) return st;
-  return run_attend(cache, params, pl, q, sel_pages, sel_count, out, lse, nullptr, ws, kAttendSparse,
-                    static_cast<cudaStream_t>(stream));
+  // the sparse mode only reads the page list
+  return run_attend(cache, params, pl, q, const_cast<int32_t*>(sel_pages), const_cast<int32_t*>(sel_count), out,
+                    lse, nullptr, ws, kAttendSparse, static_cast<cudaStream_t>(stream));
 }
 
 locks_status_t locks_decode_step(const locks_cache_t* cache, const locks_summary_t* summary,
@@ -443,8 +475,26 @@ locks_status_t locks_decode_step(const locks_cache_t* cache, const locks_summary
   int32_t* sel = sel_pages ? sel_pages : at<int32_t>(ws, pl.off_sel);
   int32_t* cnt = sel_count ? sel_count : at<int32_t>(ws, pl.off_selcnt);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (pl.fused) {
+    // the scan, then one attention kernel whose clusters select the pages
+    if ((st = run_select(cache, summary, params, pl, q, nullptr, nullptr, nullptr, ws, s)) != LOCKS_OK) return st;
+    return run_attend(cache, params, pl, q, sel, cnt, out, lse, nullptr, ws, kAttendFused, s, true);
+  }
   if ((st = run_select(cache, summary, params, pl, q, sel, cnt, nullptr, ws, s)) != LOCKS_OK) return st;
   return run_attend(cache, params, pl, q, sel, cnt, out, lse, nullptr, ws, kAttendSparse, s, true);
+}
+
+locks_status_t locks_decode_step_launches(const locks_cache_t* cache, const locks_summary_t* summary,
+                                          const locks_params_t* params, int32_t* launches) {
+  if (!launches) return LOCKS_ERR_INVALID_ARG;
+  locks_status_t st = check_cache(cache, false);
+  if (st != LOCKS_OK) return st;
+  if ((st = check_params(cache, params)) != LOCKS_OK) return st;
+  if ((st = check_summary(summary, true)) != LOCKS_OK) return st;
+  Plan pl = make_plan(cache, params);
+  if (!pl.ok) return LOCKS_ERR_UNSUPPORTED;
+  *launches = pl.fused ? 2 : 3;
+  return LOCKS_OK;
 }
 
 locks_status_t locks_dense_decode(const locks_cache_t* cache, const locks_params_t* params, const void* q,

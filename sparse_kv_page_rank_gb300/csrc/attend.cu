@@ -98,6 +98,198 @@ __device__ __forceinline__ Item get_item(const AttendArgs& a, int i, int b, int 
   return it;
 }
 
+// Fused mode: the cluster's own page selection.  Lives after the receive area
+// of the cluster merge in dynamic shared memory (same offset in every CTA, so
+// the candidate lists can be written across the cluster).
+struct FusedShared {
+  unsigned long long comb[4 * kAttendThreads];  // (key << 32) | ~page; local keys, then the filtered set
+  int phys[kAttendThreads];                     // physical page of each local key
+  float z[16];                                  // Z_h (natural log) per head
+  unsigned long long sel_comb[kFusedMaxK];
+  int sel_phys[kFusedMaxK];
+  int fsel_lp[kFusedMaxK], fsel_phys[kFusedMaxK];  // the selection, ascending page order
+  unsigned long long thresh;
+  int f_count;
+  unsigned short f_idx[16 * kFusedMaxK];
+  uint4 cand[16][kFusedMaxK];  // every CTA's candidates: {comb lo, comb hi, phys, 0}, descending comb
+};
+
+__device__ __forceinline__ unsigned long long cand_comb(const uint4& v) {
+  return ((unsigned long long)v.y << 32) | v.x;
+}
+
+// Group-shared page scores and top-k for one (sequence, KV head) problem,
+// computed by the CS CTAs of its cluster (explainer §2 "Group-Shared
+// Selection": sigma_j = ln((1/G) sum_h exp(s_hat[h][j] - Z_h)), the k pages of
+// largest sigma, ties to the lower page).  CTA c scores pages [c ppc,
+// (c+1) ppc) (ppc <= kAttendThreads: one page per thread) and ranks them
+// against each other; its k best (key, page, physical page) go to every CTA
+// of the cluster.  Every CTA then merges the CS sorted lists the same way: a
+// lower bound T on the k-th largest key (the k-th largest of each list's first
+// ceil(k / CS) entries) filters the candidates, the survivors are ranked
+// against each other, and the k winners are put in ascending page order in
+// fs.fsel_lp / fs.fsel_phys.  Called by every thread of every CTA of the
+// cluster; cluster barrier phase 1 has been arrived at (not waited on).
+__device__ void cluster_select(const AttendArgs& a, int b, int bh, int ns, int k, int CS, uint32_t crank,
+                               FusedShared& fs) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = a.group;
+  const int ppc = (ns + CS - 1) / CS;
+  const int j = (int)crank * ppc + tid;
+  const bool valid = tid < ppc && j < ns;
+  // one round trip: this thread's s_hat row and block-table entry, and the
+  // scan partials of up to four heads per warp
+  float sv[16];
+#pragma unroll
+  for (int h = 0; h < 16; ++h) sv[h] = 0.f;
+  int phys = -1;
+  if (valid) {
+    const float* row = a.shat + ((size_t)bh * a.max_pages + j) * G;
+    if ((G & 3) == 0) {
+#pragma unroll
+      for (int h4 = 0; h4 < 4; ++h4) {
+        if (4 * h4 < G) {
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(row) + h4);
+          sv[4 * h4] = v.x;
+          sv[4 * h4 + 1] = v.y;
+          sv[4 * h4 + 2] = v.z;
+          sv[4 * h4 + 3] = v.w;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int h = 0; h < 16; ++h)
+        if (h < G) sv[h] = __ldcg(row + h);
+    }
+    phys = __ldg(a.block_table + (size_t)b * a.max_pages + j);
+  }
+  {
+    const float2* pb = a.part + (size_t)bh * a.n_scan_chunks * G;
+#pragma unroll
+    for (int hh = 0; hh < 4; ++hh) {
+      const int h = warp + 4 * hh;  // warp-uniform
+      if (h < G) {
+        float m = -INFINITY, l = 0.f;
+        for (int i = lane; i < a.n_scan_chunks; i += 32) {
+          const float2 v = __ldcg(pb + (size_t)i * G + h);
+          lse2_merge(m, l, v.x, v.y);
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+          const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+          const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
+          lse2_merge(m, l, m2, l2);
+        }
+        if (lane == 0) fs.z[h] = (m + fast_log2(l)) * kLn2;
+      }
+    }
+  }
+  __syncthreads();
+  trace_mark(a.err, kTrTopkLoaded, false);
+  // sigma_j -> order-preserving key; (key, ~page) orders by key, then lower page
+  unsigned long long mine = 0ull;
+  if (valid) {
+    const float log2G = log2f((float)G);
+    float y[16];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int h = 0; h < 16; ++h) {
+      y[h] = h < G ? fmaf(sv[h], kLog2e, -fs.z[h] * kLog2e) : -INFINITY;
+      mx = fmaxf(mx, y[h]);
+    }
+    float acc = 0.f;
+#pragma unroll
+    for (int h = 0; h < 16; ++h) acc += h < G ? fast_exp2(y[h] - mx) : 0.f;
+    const uint32_t key = orderable_key((mx + fast_log2(acc) - log2G) * kLn2);
+    mine = ((unsigned long long)key << 32) | (0xffffffffu - (uint32_t)j);
+  }
+  fs.comb[tid] = mine;  // zero for a thread without a page: below every real entry
+  fs.phys[tid] = phys;
+  __syncthreads();
+  // rank among this CTA's pages; the k best go to every CTA of the cluster
+  const int n_local = max(0, min(ns - (int)crank * ppc, ppc));
+  const int kl = min(k, n_local);
+  int rank = kAttendThreads;
+  if (valid) {
+    rank = 0;
+    const ulonglong2* c2 = reinterpret_cast<const ulonglong2*>(fs.comb);
+    for (int v = 0; v < kAttendThreads / 2; ++v) {
+      const ulonglong2 x = c2[v];
+      rank += (x.x > mine) + (x.y > mine);
+    }
+  }
+  cluster_wait();  // phase 1: every CTA of the cluster is running and set up
+  if (rank < kl) {
+    const uint4 rec = make_uint4((uint32_t)mine, (uint32_t)(mine >> 32), (uint32_t)phys, 0u);
+    const uint32_t dst = smem_u32(&fs.cand[crank][rank]);
+    for (int r = 0; r < CS; ++r) st_dsmem_u4(dsmem_addr(dst, (uint32_t)r), rec);
+  }
+  cluster_arrive();  // phase 2: release this CTA's candidate stores
+  cluster_wait();
+  trace_mark(a.err, kTrTopkKeys, false);
+  // ---- merge (identical in every CTA) ----
+  auto kl_of = [&](int c) { return min(k, max(0, min(ns - c * ppc, ppc))); };
+  const int m = (k + CS - 1) / CS;
+  int usz = 0;
+  for (int c = 0; c < CS; ++c) usz += min(m, kl_of(c));
+  unsigned long long T = 0ull;
+  if (usz >= k) {
+    // T: the k-th largest of the lists' first m entries, a lower bound on the
+    // k-th largest candidate
+    if (tid < usz) {
+      int t = tid, c = 0;
+      while (t >= min(m, kl_of(c))) {
+        t -= min(m, kl_of(c));
+        ++c;
+      }
+      const unsigned long long v = cand_comb(fs.cand[c][t]);
+      int rk = 0;
+      for (int c2 = 0; c2 < CS; ++c2) {
+        const int u = min(m, kl_of(c2));
+        for (int p2 = 0; p2 < u; ++p2) rk += cand_comb(fs.cand[c2][p2]) > v;
+      }
+      if (rk == k - 1) fs.thresh = v;
+    }
+    __syncthreads();
+    T = fs.thresh;
+  }
+  if (tid == 0) fs.f_count = 0;
+  __syncthreads();
+  for (int e = tid; e < CS * kFusedMaxK; e += kAttendThreads) {
+    const int c = e / kFusedMaxK, p = e % kFusedMaxK;
+    if (p < kl_of(c)) {
+      const unsigned long long v = cand_comb(fs.cand[c][p]);
+      if (v >= T) {
+        const int slot = atomicAdd(&fs.f_count, 1);
+        fs.f_idx[slot] = (unsigned short)e;
+        fs.comb[slot] = v;
+      }
+    }
+  }
+  __syncthreads();
+  const int nf = fs.f_count;
+  for (int f = tid; f < nf; f += kAttendThreads) {
+    const unsigned long long v = fs.comb[f];
+    int rk = 0;
+    for (int f2 = 0; f2 < nf; ++f2) rk += fs.comb[f2] > v;
+    if (rk < k) {
+      const int e = fs.f_idx[f];
+      fs.sel_comb[rk] = v;
+      fs.sel_phys[rk] = (int)fs.cand[e / kFusedMaxK][e % kFusedMaxK].z;
+    }
+  }
+  __syncthreads();
+  if (tid < k) {
+    const int lp = (int)(0xffffffffu - (uint32_t)fs.sel_comb[tid]);
+    int pos = 0;
+    for (int i = 0; i < k; ++i) pos += (int)(0xffffffffu - (uint32_t)fs.sel_comb[i]) < lp;
+    fs.fsel_lp[pos] = lp;
+    fs.fsel_phys[pos] = fs.sel_phys[tid];
+  }
+  __syncthreads();
+  trace_mark(a.err, kTrTopkSelected, false);
+}
+
 template <int MODE, int STAGES, int P>
 __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_constant__ CUtensorMap tk,
                                                                 const __grid_constant__ CUtensorMap tv,
@@ -125,23 +317,26 @@ __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_con
   const int b = bh / a.num_kv_heads, hkv = bh % a.num_kv_heads;
   const int G = a.group, Hq = a.num_kv_heads * G;
 
-  if (MODE == kAttendSparse) trace_mark(a.err, kTrAttEnter, true);
+  constexpr bool FUSED = MODE == kAttendFused;
+  constexpr bool SPL = MODE == kAttendSparse || FUSED;  // a page list, one cluster per problem
+  if (SPL) trace_mark(a.err, kTrAttEnter, true);
   if (tid == 0) {
     prefetch_tmap(&tk);
     if (MODE != kAttendPageLse) prefetch_tmap(&tv);
     for (int s = 0; s < STAGES; ++s) mbar_init(&bars[s], 1);
-    if (MODE == kAttendSparse)
-      mbar_init(reinterpret_cast<uint64_t*>(smem + STAGES * kStage + kRecvO + kRecvMl), a.cluster);
+    if (SPL) mbar_init(reinterpret_cast<uint64_t*>(smem + STAGES * kStage + kRecvO + kRecvMl), a.cluster);
     fence_mbar_init();
   }
   __syncthreads();
-  // sparse mode: every CTA's receive barrier must be initialised before any
-  // other CTA of the cluster arrives on it (the matching wait comes at the merge)
-  if (MODE == kAttendSparse) cluster_arrive();
+  // page-list modes: every CTA's receive barrier must be initialised before
+  // any other CTA of the cluster arrives on it or writes to it (the matching
+  // wait comes at the selection or at the merge)
+  if (SPL) cluster_arrive();
 
-  // Inside the fused step the step's own inputs (q, lengths, block table) were
-  // written before its first kernel started, so they can be read while the
-  // selection is still being computed; the selection itself only after the wait.
+  // Inside the fused step the step's own inputs (q, lengths, block table, the
+  // cache pages) were written before its first kernel started, so they can be
+  // read while the selection is still being computed; the selection itself
+  // only after the wait.
   if (!a.inputs_early) pdl_wait();
 
   // Q fragments (rows = heads of the group; rows >= G are zero)
@@ -159,8 +354,8 @@ __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_con
     }
   }
   int L = a.seq_lens[b];
-  const int ns_raw = (MODE == kAttendSparse) ? a.n_summarized[b] : 0;
-  if (MODE == kAttendSparse && a.inputs_early) {
+  const int ns_raw = SPL ? a.n_summarized[b] : 0;
+  if (SPL && a.inputs_early) {
     // warm L2 with this sequence's block-table row while the selection is
     // still being computed (the entries are looked up right after the wait)
     const char* row = reinterpret_cast<const char*>(a.block_table + (size_t)b * a.max_pages);
@@ -168,51 +363,71 @@ __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_con
     for (int li = tid; li < lines; li += kAttendThreads)
       asm volatile("prefetch.global.L2 [%0];\n" ::"l"(row + (size_t)li * 128));
   }
-  if (a.inputs_early) pdl_wait();
-  if (MODE == kAttendSparse) trace_mark(a.err, kTrAttWait, true);
-
-  if (L < 0 || L > a.max_pages * P) {
-    if (tid == 0 && split == 0) set_error(a.err, LOCKS_DEVERR_LENGTHS);
-    L = L < 0 ? 0 : a.max_pages * P;
-  }
-  const int n_pages = (L + P - 1) / P;
-  int ns = 0, cnt = 0, n_items;
-  if (MODE == kAttendSparse) {
-    const int cap = min(L / P, a.max_pages);
-    ns = ns_raw < 0 ? 0 : (ns_raw > cap ? cap : ns_raw);
-    cnt = a.sel_count[bh];
-    const int kcap = min(a.k_max, ns);
-    if (cnt < 0 || cnt > kcap) {
-      if (tid == 0) set_error(a.err, LOCKS_DEVERR_SEL_PAGE);
-      cnt = cnt < 0 ? 0 : kcap;
-    }
-    n_items = cnt + (n_pages - ns);
-  } else {
-    n_items = n_pages;
-  }
-  // pages per CTA: a whole number of tiles
-  const int ipc = ((n_items + a.n_splits - 1) / a.n_splits + kPPT - 1) / kPPT * kPPT;
-  const int i0 = min(n_items, split * ipc), i1 = min(n_items, i0 + ipc);
-  const int ntile = (i1 - i0 + kPPT - 1) / kPPT;
 
   const uint32_t sbase = smem_u32(smem);
   // bytes one page brings into a stage (K, and V unless page-LSE mode)
   constexpr uint32_t kPageTx = (uint32_t)P * kHeadDim * 2 * (MODE == kAttendPageLse ? 1 : 2);
+  int ns = 0, cnt = 0, n_items = 0, n_tail = 0, i0 = 0, i1 = 0, ntile = 0;
+  bool sel_needed = false;  // fused mode: more summarised pages than the budget holds
+  FusedShared* fsp = reinterpret_cast<FusedShared*>(smem + STAGES * kStage + kRecvBytes);  // fused mode only
+  auto clamp_lengths = [&]() {
+    if (L < 0 || L > a.max_pages * P) {
+      if (tid == 0 && split == 0) set_error(a.err, LOCKS_DEVERR_LENGTHS);
+      L = L < 0 ? 0 : a.max_pages * P;
+    }
+  };
+  // pages per CTA: a whole number of tiles
+  auto set_range = [&]() {
+    const int ipc = ((n_items + a.n_splits - 1) / a.n_splits + kPPT - 1) / kPPT * kPPT;
+    i0 = min(n_items, split * ipc);
+    i1 = min(n_items, i0 + ipc);
+    ntile = (i1 - i0 + kPPT - 1) / kPPT;
+  };
+  // fused mode, item i: the open tail first (pages ns, ns + 1, ...), then the
+  // selected pages in ascending order (all summarised pages when they fit)
+  auto fused_item = [&](int i) {
+    Item it;
+    it.lp = -1;
+    it.phys = 0;
+    it.len = 0;
+    int lp, phys = 0;
+    bool lookup = true;
+    if (i < n_tail) {
+      lp = ns + i;
+    } else if (sel_needed) {
+      lp = fsp->fsel_lp[i - n_tail];
+      phys = fsp->fsel_phys[i - n_tail];
+      lookup = false;
+    } else {
+      lp = i - n_tail;
+    }
+    if (lookup) phys = a.block_table[(size_t)b * a.max_pages + lp];
+    if (phys < 0 || phys >= a.pages_total) {
+      set_error(a.err, LOCKS_DEVERR_BLOCK_TABLE);
+      return it;
+    }
+    it.lp = lp;
+    it.phys = phys;
+    const int rem = L - lp * P;
+    it.len = rem < P ? rem : P;
+    return it;
+  };
   // resolve items [base, base + kAttendThreads) of this CTA: selection entry
   // and block-table entry, all threads at once
   auto resolve = [&](int base) {
     const int i = i0 + base + tid;
     const int buf = (base / kAttendThreads) & 1;
     if (i < i1) {
-      const Item it = get_item<MODE, P>(a, i, b, bh, L, ns, cnt);
+      Item it;
+      if constexpr (FUSED)
+        it = fused_item(i);
+      else
+        it = get_item<MODE, P>(a, i, b, bh, L, ns, cnt);
       it_phys[buf][tid] = it.phys;
       it_len[buf][tid] = it.len;
       it_lp[buf][tid] = it.lp;
     }
   };
-  resolve(0);
-  __syncthreads();
-  if (MODE == kAttendSparse) trace_mark(a.err, kTrAttResolved, false);
   // thread 0 only; the pages of tile t must lie in the resolved batch.
   // Page w of a tile lands in rows 16w.. of each 64-row half-tile (byte
   // offset 2048 w, a multiple of the 1024-byte swizzle period).
@@ -232,8 +447,60 @@ __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_con
       }
     }
   };
+  int n_pre = 0;  // tiles issued before the selection
+  if constexpr (FUSED) {
+    // the page list's shape depends on the lengths only (inputs of the step)
+    clamp_lengths();
+    const int n_pages = (L + P - 1) / P;
+    const int cap = min(L / P, a.max_pages);
+    ns = ns_raw < 0 ? 0 : (ns_raw > cap ? cap : ns_raw);
+    sel_needed = a.k_max > 0 && ns > a.k_max;
+    cnt = min(a.k_max, ns);
+    n_tail = n_pages - ns;
+    n_items = n_tail + cnt;
+    set_range();
+    // the open tail needs no selection: its first tiles load during the wait
+    if (i0 + tid < i1 && i0 + tid < n_tail) resolve(0);
+    __syncthreads();
+    n_pre = min(min(STAGES, ntile), max(0, n_tail - i0));
+    if (tid == 0)
+      for (int t = 0; t < n_pre; ++t) issue(t, t);
+    pdl_wait();
+    trace_mark(a.err, kTrAttWait, true);
+    if (sel_needed) cluster_select(a, b, bh, ns, a.k_max, a.cluster, cluster_ctarank(), *fsp);
+    if (i0 + tid < i1 && i0 + tid >= n_tail) resolve(0);
+    if (cluster_ctarank() == 0) {
+      // publish the page list (callers may read it back)
+      for (int i = tid; i < cnt; i += kAttendThreads)
+        a.sel_pages_out[(size_t)bh * a.k_max + i] = sel_needed ? fsp->fsel_lp[i] : i;
+      if (tid == 0) a.sel_count_out[bh] = cnt;
+    }
+    __syncthreads();
+  } else {
+    if (a.inputs_early) pdl_wait();
+    if (SPL) trace_mark(a.err, kTrAttWait, true);
+    clamp_lengths();
+    const int n_pages = (L + P - 1) / P;
+    if (MODE == kAttendSparse) {
+      const int cap = min(L / P, a.max_pages);
+      ns = ns_raw < 0 ? 0 : (ns_raw > cap ? cap : ns_raw);
+      cnt = a.sel_count[bh];
+      const int kcap = min(a.k_max, ns);
+      if (cnt < 0 || cnt > kcap) {
+        if (tid == 0) set_error(a.err, LOCKS_DEVERR_SEL_PAGE);
+        cnt = cnt < 0 ? 0 : kcap;
+      }
+      n_items = cnt + (n_pages - ns);
+    } else {
+      n_items = n_pages;
+    }
+    set_range();
+    resolve(0);
+    __syncthreads();
+  }
+  if (SPL) trace_mark(a.err, kTrAttResolved, false);
   if (tid == 0) {
-    for (int s = 0; s < STAGES && s < ntile; ++s) issue(s, s);
+    for (int s = n_pre; s < STAGES && s < ntile; ++s) issue(s, s);
   }
 
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
@@ -258,7 +525,7 @@ __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_con
       break;
     }
     consumed = it + 1;
-    if (MODE == kAttendSparse && it == 0) trace_mark(a.err, kTrAttFirstData, false);
+    if (SPL && it == 0) trace_mark(a.err, kTrAttFirstData, false);
     const uint32_t kb = sbase + stage * kStage;
     const uint32_t vb = kb + kTile;
 
@@ -405,7 +672,7 @@ __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_con
   }
   pdl_launch_dependents();
   if (MODE == kAttendPageLse) return;
-  if (MODE == kAttendSparse) trace_mark(a.err, kTrAttLooped, false);
+  if (SPL) trace_mark(a.err, kTrAttLooped, false);
 
   // ---- merge the four warps of this CTA ----
   l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
@@ -460,11 +727,11 @@ __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_con
   }
   __syncthreads();
 
-  if (MODE == kAttendSparse) trace_mark(a.err, kTrAttCtaMerged, false);
+  if (SPL) trace_mark(a.err, kTrAttCtaMerged, false);
   // ---- merge the CTAs of the cluster through distributed shared memory ----
   const int CS = a.cluster, NC = a.n_splits / a.cluster;
   const uint32_t rank = cluster_ctarank();
-  if (MODE == kAttendSparse) {
+  if (SPL) {
     // One cluster per problem.  Each CTA pushes its partial state to the
     // CTAs that own its output columns (rank r owns columns [r*cols,
     // (r+1)*cols)) and arrives on their receive barriers; each CTA then
@@ -475,7 +742,9 @@ __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_con
     float* recv_o = reinterpret_cast<float*>(smem + STAGES * kStage);
     float2* recv_ml = reinterpret_cast<float2*>(smem + STAGES * kStage + kRecvO);
     uint64_t* recv_bar = reinterpret_cast<uint64_t*>(smem + STAGES * kStage + kRecvO + kRecvMl);
-    cluster_wait();  // every CTA's receive barrier is initialised
+    // every CTA's receive barrier is initialised (already waited for when the
+    // cluster selected the pages itself)
+    if (!(FUSED && sel_needed)) cluster_wait();
     const uint32_t ro = smem_u32(recv_o), rml = smem_u32(recv_ml);
     for (int e = tid; e < G * (kHeadDim / 4); e += kAttendThreads) {
       const int h = e / (kHeadDim / 4), c4 = 4 * (e % (kHeadDim / 4));
@@ -490,7 +759,7 @@ __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_con
     __syncthreads();  // the whole CTA's stores precede the release arrivals
     if (tid < CS) mbar_arrive_remote(dsmem_addr(smem_u32(recv_bar), tid));
     if (!mbar_wait_cluster(recv_bar, 0) && tid == 0) set_error(a.err, kDevErrTimeout);
-    if (MODE == kAttendSparse) trace_mark(a.err, kTrAttClusterMerged, false);
+    if (SPL) trace_mark(a.err, kTrAttClusterMerged, false);
     for (int e = tid; e < G * cols; e += kAttendThreads) {
       const int h = e / cols, cc = e % cols, col = (int)rank * cols + cc;
       float M = -INFINITY;
@@ -509,7 +778,7 @@ __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_con
       a.out[oi * kHeadDim + col] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
       if (a.lse && col == 0) a.lse[oi] = (Ls > 0.f) ? (M + fast_log2(Ls)) * kLn2 : -INFINITY;
     }
-    if (MODE == kAttendSparse) trace_mark(a.err, kTrAttExit, false);
+    if (SPL) trace_mark(a.err, kTrAttExit, false);
     return;
   }
   const int q = split / CS;
@@ -555,9 +824,9 @@ __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_con
     }
   }
   if (NC == 1) {
-    if (MODE == kAttendSparse) trace_mark(a.err, kTrAttClusterMerged, false);
+    if (SPL) trace_mark(a.err, kTrAttClusterMerged, false);
     cluster_sync();  // no CTA leaves while others still read its shared memory
-    if (MODE == kAttendSparse) trace_mark(a.err, kTrAttExit, false);
+    if (SPL) trace_mark(a.err, kTrAttExit, false);
     return;
   }
 
@@ -595,7 +864,8 @@ __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_con
 
 template <int MODE, int STAGES>
 size_t smem_bytes() {
-  return (size_t)STAGES * kStage + 1024 + (MODE == kAttendSparse ? kRecvBytes : 0);
+  return (size_t)STAGES * kStage + 1024 + (MODE == kAttendSparse ? kRecvBytes : 0) +
+         (MODE == kAttendFused ? kRecvBytes + sizeof(FusedShared) : 0);
 }
 
 template <int MODE, int STAGES, int P>
@@ -688,42 +958,51 @@ int max_cluster_of() {
 
 constexpr int kSparseStages = 3;
 constexpr int kDenseStages = 2;
+// fused: two stages keep two CTAs per SM with the selection's shared memory
+// (each CTA of a problem's cluster holds about two selected pages)
+constexpr int kFusedStages = 2;
+
+// index of a mode in the occupancy caches
+int mode_slot(int mode) { return mode == kAttendSparse ? 0 : (mode == kAttendFused ? 2 : 1); }
 
 }  // namespace
 
 int attend_active_clusters(int mode, int cs, int page_size) {
-  static int cache[2][2][5][64] = {};
+  static int cache[2][3][5][64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || cs < 1 || cs > 16) return 1;
-  const int m = mode == kAttendSparse ? 0 : 1, p16 = page_size == 16 ? 1 : 0;
+  const int m = mode_slot(mode), p16 = page_size == 16 ? 1 : 0;
+  if (m == 2 && p16) return 0;
   const int li = 31 - __builtin_clz((unsigned)cs);
   int& slot = cache[p16][m][li][dev];
   if (slot == 0) {
     int n;
     if (p16)
-      n = mode == kAttendSparse ? active_clusters_of<kAttendSparse, kSparseStages, 16>(cs)
-                                : active_clusters_of<kAttendDense, kDenseStages, 16>(cs);
+      n = m == 0 ? active_clusters_of<kAttendSparse, kSparseStages, 16>(cs)
+                 : active_clusters_of<kAttendDense, kDenseStages, 16>(cs);
     else
-      n = mode == kAttendSparse ? active_clusters_of<kAttendSparse, kSparseStages, kPage>(cs)
-                                : active_clusters_of<kAttendDense, kDenseStages, kPage>(cs);
+      n = m == 0   ? active_clusters_of<kAttendSparse, kSparseStages, kPage>(cs)
+          : m == 2 ? active_clusters_of<kAttendFused, kFusedStages, kPage>(cs)
+                   : active_clusters_of<kAttendDense, kDenseStages, kPage>(cs);
     slot = n > 0 ? n : -1;
   }
   return slot > 0 ? slot : 0;
 }
 
 int attend_max_cluster(int mode, int page_size) {
-  static int cache[2][2][64] = {};
+  static int cache[2][3][64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 8;
-  const int m = mode == kAttendSparse ? 0 : 1, p16 = page_size == 16 ? 1 : 0;
+  const int m = mode_slot(mode), p16 = page_size == 16 ? 1 : 0;
+  if (m == 2 && p16) return 1;
   int& slot = cache[p16][m][dev];
   if (slot == 0) {
     if (p16)
-      slot = mode == kAttendSparse ? max_cluster_of<kAttendSparse, kSparseStages, 16>()
-                                   : max_cluster_of<kAttendDense, kDenseStages, 16>();
+      slot = m == 0 ? max_cluster_of<kAttendSparse, kSparseStages, 16>() : max_cluster_of<kAttendDense, kDenseStages, 16>();
     else
-      slot = mode == kAttendSparse ? max_cluster_of<kAttendSparse, kSparseStages, kPage>()
-                                   : max_cluster_of<kAttendDense, kDenseStages, kPage>();
+      slot = m == 0   ? max_cluster_of<kAttendSparse, kSparseStages, kPage>()
+             : m == 2 ? max_cluster_of<kAttendFused, kFusedStages, kPage>()
+                      : max_cluster_of<kAttendDense, kDenseStages, kPage>();
   }
   return slot;
 }
@@ -734,6 +1013,9 @@ cudaError_t launch_page(const AttendArgs& a, const CUtensorMap& tk, const CUtens
   switch (mode) {
     case kAttendSparse: return launch_mode<kAttendSparse, kSparseStages, P>(a, tk, tv, s, pdl);
     case kAttendDense: return launch_mode<kAttendDense, kDenseStages, P>(a, tk, tv, s, pdl);
+    case kAttendFused:
+      if constexpr (P == kPage) return launch_mode<kAttendFused, kFusedStages, P>(a, tk, tv, s, pdl);
+      return cudaErrorInvalidValue;  // 64-token pages only
     default: return launch_mode<kAttendPageLse, kDenseStages, P>(a, tk, tv, s, pdl);
   }
 }

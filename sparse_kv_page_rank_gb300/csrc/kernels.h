@@ -67,9 +67,20 @@ struct AttendArgs {
   int inputs_early;           // 1: the step's inputs may be read before the grid dependency wait
   float scale_log2;
   int page_size;              // P: 64 (one page per 64-token tile) or 16 (four pages per tile)
+  // fused mode only: the scan's page-mass estimates and per-CTA partials,
+  // from which the cluster selects the pages itself
+  const float* shat;          // ws: [B*Hkv][max_pages][G] natural log
+  const float2* part;         // ws: [B*Hkv][n_scan_chunks][G] (max, sum) of base-2 LSE
+  int n_scan_chunks;
+  int32_t* sel_pages_out;     // fused mode: the page list it selected, [B*Hkv][k_max] (as locks_select)
+  int32_t* sel_count_out;     // fused mode: [B*Hkv]
 };
 
-enum AttendMode { kAttendSparse = 0, kAttendDense = 1, kAttendPageLse = 2 };
+// kAttendFused: the sparse mode with the group-shared top-k computed inside
+// the thread-block cluster from the scan's outputs (64-token pages, k_max <=
+// kFusedMaxK, at most kAttendThreads summarised pages per CTA of the cluster).
+enum AttendMode { kAttendSparse = 0, kAttendDense = 1, kAttendPageLse = 2, kAttendFused = 3 };
+constexpr int kFusedMaxK = 32;
 
 // Summary builder.
 struct BuildArgs {
@@ -92,6 +103,7 @@ cudaError_t launch_build(const BuildArgs& a, cudaStream_t s);
 size_t topk_smem_bytes(size_t keys);
 int topk_pages_per_cta(int group);  // pages one top-k CTA scores
 int attend_max_cluster(int mode, int page_size);  // largest placeable cluster (<= 16) for that mode
+                                                  // (kAttendFused: page_size 64 only)
 int attend_active_clusters(int mode, int cs, int page_size);  // clusters of cs CTAs resident at once
 // Scan CTA: 7 consumer warps + 1 producer warp, so that two CTAs put four
 // warps on each SM sub-partition (whose register file is a quarter of the SM's).

@@ -29,6 +29,7 @@ LOCKS_STATIC_WS_BYTES = 8 << 20
 LOCKS_DTYPE_BF16 = 0
 LOCKS_DTYPE_F32 = 1
 LOCKS_DTYPE_Q4 = 2
+LOCKS_FLAG_UNFUSED = 0x1
 
 
 def q4_page_head_bytes(rank: int, page_size: int = 64) -> int:
@@ -89,6 +90,7 @@ def lib() -> ctypes.CDLL:
             "locks_page_scores": (ctypes.c_int, [C, S, R, vp, vp, vp, sz, vp]),
             "locks_sparse_attend": (ctypes.c_int, [C, R, vp, vp, vp, vp, vp, vp, sz, vp]),
             "locks_decode_step": (ctypes.c_int, [C, S, R, vp, vp, vp, vp, vp, vp, sz, vp]),
+            "locks_decode_step_launches": (ctypes.c_int, [C, S, R, P(i32)]),
             "locks_dense_decode": (ctypes.c_int, [C, R, vp, vp, vp, vp, sz, vp]),
             "locks_exact_page_lse": (ctypes.c_int, [C, R, vp, vp, vp]),
             "locks_get_device_error": (ctypes.c_int, [vp, P(i32), vp]),
@@ -201,6 +203,13 @@ def locks_decode_step_static(cache, summary, params, q, out, lse, sel_pages=None
     _check(lib().locks_decode_step_static(ctypes.byref(cache), ctypes.byref(summary), ctypes.byref(params),
                                           _ptr(q), _ptr(out), _ptr(lse), _ptr(sel_pages), _ptr(sel_count),
                                           _ptr(device_error), _stream(stream)), "locks_decode_step_static")
+
+
+def locks_decode_step_launches(cache, summary, params) -> int:
+    n = ctypes.c_int32(0)
+    _check(lib().locks_decode_step_launches(ctypes.byref(cache), ctypes.byref(summary), ctypes.byref(params),
+                                            ctypes.byref(n)), "locks_decode_step_launches")
+    return n.value
 
 
 def locks_dense_decode(cache, params, q, out, lse, ws, ws_bytes: int, stream=None):

@@ -20,11 +20,12 @@ class LocksRuntime:
     Summaries are allocated here: bf16 [pages_total][Hkv][rank][128] and
     [..][P][rank], or, with ``quantized``, one packed LOCKS_DTYPE_Q4 block per
     page-head (uint8 [pages_total][Hkv][q4_page_head_bytes(rank, P)]).
+    ``unfused`` sets LOCKS_FLAG_UNFUSED (the decode step as three kernels).
     """
 
     def __init__(self, k_pool: torch.Tensor, v_pool: torch.Tensor, block_table: torch.Tensor,
                  seq_lens: torch.Tensor, n_summarized: torch.Tensor, num_q_heads: int, rank: int,
-                 budget_tokens: int, scale: float = 0.0, quantized: bool = False):
+                 budget_tokens: int, scale: float = 0.0, quantized: bool = False, unfused: bool = False):
         assert k_pool.dtype == torch.bfloat16 and v_pool.dtype == torch.bfloat16
         assert block_table.dtype == torch.int32 and seq_lens.dtype == torch.int32
         self.device = k_pool.device
@@ -46,7 +47,8 @@ class LocksRuntime:
         self.cache = L.make_cache(k_pool, v_pool, block_table, seq_lens, self.n_summarized)
         self.summary = L.make_summary(self.basis_t, self.coeffs, rank,
                                       L.LOCKS_DTYPE_Q4 if quantized else L.LOCKS_DTYPE_BF16)
-        self.params = L.make_params(num_q_heads, budget_tokens, scale)
+        self.params = L.make_params(num_q_heads, budget_tokens, scale,
+                                    L.LOCKS_FLAG_UNFUSED if unfused else 0)
         self.k_max = min(budget_tokens // P, block_table.shape[1])
         self.ws_bytes = L.locks_workspace_size(self.cache, self.summary, self.params)
         self.ws = torch.empty(self.ws_bytes + 256, dtype=torch.uint8, device=self.device)
@@ -91,6 +93,10 @@ class LocksRuntime:
         L.locks_decode_step(self.cache, self.summary, self.params, q, out, lse, sp, sc, self.ws,
                             self.ws_bytes, stream)
         return out, lse
+
+    def decode_step_launches(self) -> int:
+        """Kernels one decode_step launches for this cache's shapes (2 or 3)."""
+        return L.locks_decode_step_launches(self.cache, self.summary, self.params)
 
     def dense_decode(self, q: torch.Tensor, out=None, lse=None, stream=None):
         out = self.out if out is None else out

@@ -99,7 +99,7 @@ def test_bad_cache_rejected(lib, kw, status):
     (L.make_params(7, 512), L.LOCKS_ERR_INVALID_ARG),      # not a multiple of Hkv
     (L.make_params(34, 512), L.LOCKS_ERR_UNSUPPORTED),     # G = 17
     (L.make_params(8, -1), L.LOCKS_ERR_INVALID_ARG),
-    (L.make_params(8, 512, flags=1), L.LOCKS_ERR_INVALID_ARG),
+    (L.make_params(8, 512, flags=2), L.LOCKS_ERR_INVALID_ARG),      # a reserved flag bit
     (L.make_params(8, 512, scale=-1.0), L.LOCKS_ERR_INVALID_ARG),
 ])
 def test_bad_params_rejected(lib, params, status):
