@@ -159,15 +159,19 @@ typedef struct locks_params {
   int32_t num_q_heads;
   int32_t budget_tokens;
   float scale;     /* 0 -> 1/sqrt(head_dim) */
-  int32_t flags;   /* 0 or LOCKS_FLAG_UNFUSED; other bits are reserved and must be 0 */
+  int32_t flags;   /* 0, LOCKS_FLAG_UNFUSED or LOCKS_FLAG_FUSED; other bits are reserved and must be 0 */
 } locks_params_t;
 
-/* locks_decode_step normally runs as two kernels when page_size is 64, k_max
- * <= 32 and max_pages <= 128 x (the largest thread-block cluster, 16 CTAs):
- * the summary scan, then one attention kernel whose clusters compute the
- * group-shared top-k themselves.  This flag makes it run the three-kernel
- * form (scan, top-k, attention) instead; both select the same pages. */
+/* locks_decode_step runs as two kernels when page_size is 64, k_max <= 32,
+ * max_pages <= 128 x (the largest thread-block cluster, 16 CTAs) and there
+ * are more (sequence, KV head) problems than SMs: the summary scan, then one
+ * attention kernel whose clusters compute the group-shared top-k themselves.
+ * Otherwise it runs three kernels (scan, top-k, attention).  Both forms
+ * select the same pages.  LOCKS_FLAG_UNFUSED always takes the three-kernel
+ * form; LOCKS_FLAG_FUSED takes the two-kernel form whenever the size limits
+ * allow, whatever the number of problems.  Setting both is an error. */
 #define LOCKS_FLAG_UNFUSED 0x1
+#define LOCKS_FLAG_FUSED 0x2
 
 /* Human-readable name of a status code (static string). */
 LOCKS_API const char* locks_status_string(locks_status_t status);

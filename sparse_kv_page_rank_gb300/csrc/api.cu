@@ -65,7 +65,8 @@ locks_status_t check_params(const locks_cache_t* c, const locks_params_t* p) {
   if (p->num_q_heads <= 0 || p->num_q_heads % c->num_kv_heads) return LOCKS_ERR_INVALID_ARG;
   const int G = p->num_q_heads / c->num_kv_heads;
   if (G > 16) return LOCKS_ERR_UNSUPPORTED;
-  if (p->budget_tokens < 0 || (p->flags & ~LOCKS_FLAG_UNFUSED) != 0) return LOCKS_ERR_INVALID_ARG;
+  if (p->budget_tokens < 0 || (p->flags & ~(LOCKS_FLAG_UNFUSED | LOCKS_FLAG_FUSED)) != 0) return LOCKS_ERR_INVALID_ARG;
+  if ((p->flags & LOCKS_FLAG_UNFUSED) && (p->flags & LOCKS_FLAG_FUSED)) return LOCKS_ERR_INVALID_ARG;
   if (!(p->scale >= 0.f) || !std::isfinite(p->scale)) return LOCKS_ERR_INVALID_ARG;
   return LOCKS_OK;
 }
@@ -158,8 +159,14 @@ Plan make_plan(const locks_cache_t* c, const locks_params_t* p) {
     pl.lse_splits = (int)std::max<long long>(1, std::min<long long>(ls, max_tiles));
     // fused step (64-token pages, k <= kFusedMaxK): one cluster per problem
     // whose CTAs score at most one page per thread; sized like the sparse
-    // cluster, then raised until the pages fit
-    if (P == kPage && pl.k_max <= kFusedMaxK && !(p->flags & LOCKS_FLAG_UNFUSED)) {
+    // cluster, then raised until the pages fit.  Taken when there are more
+    // problems than SMs: the separate top-k (one 512-thread CTA per SM) would
+    // then need more than one wave, while with few problems its 16 warps per
+    // CTA select faster than the 4-warp attention CTAs do (measured on GB300:
+    // 128K context, 8 problems, 24.6 us with the separate top-k and 27.6 us
+    // fused; 8K context, 256 problems, 62.7 us and 59.7 us).
+    if (P == kPage && pl.k_max <= kFusedMaxK && !(p->flags & LOCKS_FLAG_UNFUSED) &&
+        (BH > sms || (p->flags & LOCKS_FLAG_FUSED))) {
       const int cs_max = attend_max_cluster(kAttendFused, P);
       const long long need = ((long long)c->max_pages + kAttendThreads - 1) / kAttendThreads;
       int csf = 1;
@@ -326,6 +333,9 @@ locks_status_t run_attend(const locks_cache_t* c, const locks_params_t* p, const
   a.n_scan_chunks = pl.n_scan;
   a.sel_pages_out = nullptr;
   a.sel_count_out = nullptr;
+  a.k_pool16 = static_cast<const uint16_t*>(c->k_pool);
+  a.v_pool16 = static_cast<const uint16_t*>(c->v_pool);
+  a.trace_cta = nullptr;
   if (mode == kAttendSparse) {
     a.cluster = pl.sparse_cluster;
     a.n_splits = pl.sparse_cluster;
@@ -347,6 +357,16 @@ locks_status_t run_attend(const locks_cache_t* c, const locks_params_t* p, const
   }
   a.scale_log2 = scale_of(p) * kLog2e;
   a.inputs_early = inputs_early ? 1 : 0;
+#if LOCKS_TRACE
+  // tracing builds: per-CTA timestamps of the page-list modes go to the end
+  // of the workspace (the dense partials' region, the last one) when that
+  // region is large enough
+  {
+    const size_t need = sizeof(unsigned long long) * pl.BH * a.n_splits * 16;
+    if (ws && (mode == kAttendSparse || mode == kAttendFused) && pl.total - pl.off_po >= need)
+      a.trace_cta = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(ws) + pl.total - need);
+  }
+#endif
   a.page_size = c->page_size;
   return cuda_status(launch_attend(a, tk, tv, mode, st, true));
 }

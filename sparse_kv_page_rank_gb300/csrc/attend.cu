@@ -98,6 +98,20 @@ __device__ __forceinline__ Item get_item(const AttendArgs& a, int i, int b, int 
   return it;
 }
 
+// Tracing builds: this CTA's timestamp for `slot` (0..15) of the page-list modes.
+__device__ __forceinline__ void trace_cta(const AttendArgs& a, int slot) {
+#if LOCKS_TRACE
+  if (threadIdx.x == 0 && a.trace_cta) {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    a.trace_cta[((size_t)blockIdx.y * gridDim.x + blockIdx.x) * 16 + slot] = t;
+  }
+#else
+  (void)a;
+  (void)slot;
+#endif
+}
+
 // Fused mode: the cluster's own page selection.  Lives after the receive area
 // of the cluster merge in dynamic shared memory (same offset in every CTA, so
 // the candidate lists can be written across the cluster).
@@ -186,6 +200,7 @@ __device__ void cluster_select(const AttendArgs& a, int b, int bh, int ns, int k
   }
   __syncthreads();
   trace_mark(a.err, kTrTopkLoaded, false);
+  trace_cta(a, 2);
   // sigma_j -> order-preserving key; (key, ~page) orders by key, then lower page
   unsigned long long mine = 0ull;
   if (valid) {
@@ -206,6 +221,8 @@ __device__ void cluster_select(const AttendArgs& a, int b, int bh, int ns, int k
   fs.comb[tid] = mine;  // zero for a thread without a page: below every real entry
   fs.phys[tid] = phys;
   __syncthreads();
+  trace_mark(a.err, kTrSelMinMax, false);
+  trace_cta(a, 3);
   // rank among this CTA's pages; the k best go to every CTA of the cluster
   const int n_local = max(0, min(ns - (int)crank * ppc, ppc));
   const int kl = min(k, n_local);
@@ -213,12 +230,24 @@ __device__ void cluster_select(const AttendArgs& a, int b, int bh, int ns, int k
   if (valid) {
     rank = 0;
     const ulonglong2* c2 = reinterpret_cast<const ulonglong2*>(fs.comb);
+#pragma unroll 8
     for (int v = 0; v < kAttendThreads / 2; ++v) {
       const ulonglong2 x = c2[v];
       rank += (x.x > mine) + (x.y > mine);
     }
   }
+  // the CTA's few best pages are likely selected: start bringing their K and
+  // V into L2 now, while the cluster agrees on the selection
+  if (rank < kFusedPrefetch && rank < kl && phys >= 0 && phys < a.pages_total) {
+    const size_t ph = ((size_t)phys * a.num_kv_heads + (size_t)(bh % a.num_kv_heads)) * kPage * kHeadDim;
+    prefetch_l2_bulk(a.k_pool16 + ph, kPage * kHeadDim * 2);
+    prefetch_l2_bulk(a.v_pool16 + ph, kPage * kHeadDim * 2);
+  }
+  trace_mark(a.err, kTrSelRadix, false);
+  trace_cta(a, 4);
   cluster_wait();  // phase 1: every CTA of the cluster is running and set up
+  trace_mark(a.err, kTrSelCompact, false);
+  trace_cta(a, 5);
   if (rank < kl) {
     const uint4 rec = make_uint4((uint32_t)mine, (uint32_t)(mine >> 32), (uint32_t)phys, 0u);
     const uint32_t dst = smem_u32(&fs.cand[crank][rank]);
@@ -227,43 +256,64 @@ __device__ void cluster_select(const AttendArgs& a, int b, int bh, int ns, int k
   cluster_arrive();  // phase 2: release this CTA's candidate stores
   cluster_wait();
   trace_mark(a.err, kTrTopkKeys, false);
+  trace_cta(a, 6);
   // ---- merge (identical in every CTA) ----
+  // T = the k-th largest of the lists' first m entries (m as large as keeps
+  // one entry per thread) is a lower bound on the k-th largest candidate;
+  // the candidates >= T are then ranked against each other.
   auto kl_of = [&](int c) { return min(k, max(0, min(ns - c * ppc, ppc))); };
-  const int m = (k + CS - 1) / CS;
+  const int m = min(k, kAttendThreads / CS);
   int usz = 0;
   for (int c = 0; c < CS; ++c) usz += min(m, kl_of(c));
+  unsigned long long uv = 0ull;
+  if (tid < usz) {
+    int t = tid, c = 0;
+    while (t >= min(m, kl_of(c))) {
+      t -= min(m, kl_of(c));
+      ++c;
+    }
+    uv = cand_comb(fs.cand[c][t]);
+  }
+  fs.comb[tid] = uv;
+  if (tid == 0) fs.f_count = 0;
+  __syncthreads();
   unsigned long long T = 0ull;
   if (usz >= k) {
-    // T: the k-th largest of the lists' first m entries, a lower bound on the
-    // k-th largest candidate
     if (tid < usz) {
-      int t = tid, c = 0;
-      while (t >= min(m, kl_of(c))) {
-        t -= min(m, kl_of(c));
-        ++c;
-      }
-      const unsigned long long v = cand_comb(fs.cand[c][t]);
       int rk = 0;
-      for (int c2 = 0; c2 < CS; ++c2) {
-        const int u = min(m, kl_of(c2));
-        for (int p2 = 0; p2 < u; ++p2) rk += cand_comb(fs.cand[c2][p2]) > v;
+      const ulonglong2* c2 = reinterpret_cast<const ulonglong2*>(fs.comb);
+#pragma unroll 8
+      for (int v = 0; v < kAttendThreads / 2; ++v) {
+        const ulonglong2 x = c2[v];
+        rk += (x.x > uv) + (x.y > uv);
       }
-      if (rk == k - 1) fs.thresh = v;
+      if (rk == k - 1) fs.thresh = uv;
     }
     __syncthreads();
     T = fs.thresh;
   }
-  if (tid == 0) fs.f_count = 0;
-  __syncthreads();
-  for (int e = tid; e < CS * kFusedMaxK; e += kAttendThreads) {
-    const int c = e / kFusedMaxK, p = e % kFusedMaxK;
-    if (p < kl_of(c)) {
-      const unsigned long long v = cand_comb(fs.cand[c][p]);
-      if (v >= T) {
-        const int slot = atomicAdd(&fs.f_count, 1);
-        fs.f_idx[slot] = (unsigned short)e;
-        fs.comb[slot] = v;
+  trace_mark(a.err, kTrSelPasses, false);
+  trace_cta(a, 7);
+  // compact the candidates >= T (warp-aggregated slots)
+  for (int e0 = 0; e0 < CS * kFusedMaxK; e0 += kAttendThreads) {
+    const int e = e0 + tid;
+    bool keep = false;
+    unsigned long long v = 0ull;
+    if (e < CS * kFusedMaxK) {
+      const int c = e / kFusedMaxK, p = e % kFusedMaxK;
+      if (p < kl_of(c)) {
+        v = cand_comb(fs.cand[c][p]);
+        keep = v >= T;
       }
+    }
+    const unsigned msk = __ballot_sync(0xffffffffu, keep);
+    int base = 0;
+    if (lane == 0 && msk) base = atomicAdd(&fs.f_count, __popc(msk));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    if (keep) {
+      const int slot = base + __popc(msk & ((1u << lane) - 1u));
+      fs.comb[slot] = v;
+      fs.f_idx[slot] = (unsigned short)e;
     }
   }
   __syncthreads();
@@ -279,6 +329,8 @@ __device__ void cluster_select(const AttendArgs& a, int b, int bh, int ns, int k
     }
   }
   __syncthreads();
+  trace_mark(a.err, kTrSelCalls, false);
+  trace_cta(a, 8);
   if (tid < k) {
     const int lp = (int)(0xffffffffu - (uint32_t)fs.sel_comb[tid]);
     int pos = 0;
@@ -320,6 +372,7 @@ __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_con
   constexpr bool FUSED = MODE == kAttendFused;
   constexpr bool SPL = MODE == kAttendSparse || FUSED;  // a page list, one cluster per problem
   if (SPL) trace_mark(a.err, kTrAttEnter, true);
+  trace_cta(a, 0);
   if (tid == 0) {
     prefetch_tmap(&tk);
     if (MODE != kAttendPageLse) prefetch_tmap(&tv);
@@ -467,6 +520,7 @@ __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_con
       for (int t = 0; t < n_pre; ++t) issue(t, t);
     pdl_wait();
     trace_mark(a.err, kTrAttWait, true);
+    trace_cta(a, 1);
     if (sel_needed) cluster_select(a, b, bh, ns, a.k_max, a.cluster, cluster_ctarank(), *fsp);
     if (i0 + tid < i1 && i0 + tid >= n_tail) resolve(0);
     if (cluster_ctarank() == 0) {
@@ -499,6 +553,7 @@ __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_con
     __syncthreads();
   }
   if (SPL) trace_mark(a.err, kTrAttResolved, false);
+  trace_cta(a, 9);
   if (tid == 0) {
     for (int s = n_pre; s < STAGES && s < ntile; ++s) issue(s, s);
   }
@@ -526,6 +581,7 @@ __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_con
     }
     consumed = it + 1;
     if (SPL && it == 0) trace_mark(a.err, kTrAttFirstData, false);
+    if (SPL && it == 0) trace_cta(a, 10);
     const uint32_t kb = sbase + stage * kStage;
     const uint32_t vb = kb + kTile;
 
@@ -673,6 +729,7 @@ __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_con
   pdl_launch_dependents();
   if (MODE == kAttendPageLse) return;
   if (SPL) trace_mark(a.err, kTrAttLooped, false);
+  trace_cta(a, 11);
 
   // ---- merge the four warps of this CTA ----
   l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
@@ -728,6 +785,7 @@ __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_con
   __syncthreads();
 
   if (SPL) trace_mark(a.err, kTrAttCtaMerged, false);
+  trace_cta(a, 12);
   // ---- merge the CTAs of the cluster through distributed shared memory ----
   const int CS = a.cluster, NC = a.n_splits / a.cluster;
   const uint32_t rank = cluster_ctarank();
@@ -760,6 +818,7 @@ __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_con
     if (tid < CS) mbar_arrive_remote(dsmem_addr(smem_u32(recv_bar), tid));
     if (!mbar_wait_cluster(recv_bar, 0) && tid == 0) set_error(a.err, kDevErrTimeout);
     if (SPL) trace_mark(a.err, kTrAttClusterMerged, false);
+    trace_cta(a, 13);
     for (int e = tid; e < G * cols; e += kAttendThreads) {
       const int h = e / cols, cc = e % cols, col = (int)rank * cols + cc;
       float M = -INFINITY;
@@ -779,6 +838,7 @@ __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_con
       if (a.lse && col == 0) a.lse[oi] = (Ls > 0.f) ? (M + fast_log2(Ls)) * kLn2 : -INFINITY;
     }
     if (SPL) trace_mark(a.err, kTrAttExit, false);
+    trace_cta(a, 14);
     return;
   }
   const int q = split / CS;
@@ -825,8 +885,10 @@ __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_con
   }
   if (NC == 1) {
     if (SPL) trace_mark(a.err, kTrAttClusterMerged, false);
+    trace_cta(a, 13);
     cluster_sync();  // no CTA leaves while others still read its shared memory
     if (SPL) trace_mark(a.err, kTrAttExit, false);
+    trace_cta(a, 14);
     return;
   }
 

@@ -72,8 +72,11 @@ struct AttendArgs {
   const float* shat;          // ws: [B*Hkv][max_pages][G] natural log
   const float2* part;         // ws: [B*Hkv][n_scan_chunks][G] (max, sum) of base-2 LSE
   int n_scan_chunks;
+  const uint16_t* k_pool16;   // fused mode: pool bases for L2 prefetches of likely pages
+  const uint16_t* v_pool16;
   int32_t* sel_pages_out;     // fused mode: the page list it selected, [B*Hkv][k_max] (as locks_select)
   int32_t* sel_count_out;     // fused mode: [B*Hkv]
+  unsigned long long* trace_cta;  // tracing builds only: per-CTA timestamps [B*Hkv][n_splits][16], or null
 };
 
 // kAttendFused: the sparse mode with the group-shared top-k computed inside
@@ -81,6 +84,7 @@ struct AttendArgs {
 // kFusedMaxK, at most kAttendThreads summarised pages per CTA of the cluster).
 enum AttendMode { kAttendSparse = 0, kAttendDense = 1, kAttendPageLse = 2, kAttendFused = 3 };
 constexpr int kFusedMaxK = 32;
+constexpr int kFusedPrefetch = 4;  // each CTA's best pages whose K/V are prefetched into L2 before the merge
 
 // Summary builder.
 struct BuildArgs {

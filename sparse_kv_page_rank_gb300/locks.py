@@ -30,6 +30,7 @@ LOCKS_DTYPE_BF16 = 0
 LOCKS_DTYPE_F32 = 1
 LOCKS_DTYPE_Q4 = 2
 LOCKS_FLAG_UNFUSED = 0x1
+LOCKS_FLAG_FUSED = 0x2
 
 
 def q4_page_head_bytes(rank: int, page_size: int = 64) -> int:

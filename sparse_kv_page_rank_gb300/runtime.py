@@ -20,12 +20,13 @@ class LocksRuntime:
     Summaries are allocated here: bf16 [pages_total][Hkv][rank][128] and
     [..][P][rank], or, with ``quantized``, one packed LOCKS_DTYPE_Q4 block per
     page-head (uint8 [pages_total][Hkv][q4_page_head_bytes(rank, P)]).
-    ``unfused`` sets LOCKS_FLAG_UNFUSED (the decode step as three kernels).
+    ``form``: "auto", or "unfused" / "fused" for LOCKS_FLAG_UNFUSED / LOCKS_FLAG_FUSED
+    (the decode step as three kernels, or as two wherever the size limits allow).
     """
 
     def __init__(self, k_pool: torch.Tensor, v_pool: torch.Tensor, block_table: torch.Tensor,
                  seq_lens: torch.Tensor, n_summarized: torch.Tensor, num_q_heads: int, rank: int,
-                 budget_tokens: int, scale: float = 0.0, quantized: bool = False, unfused: bool = False):
+                 budget_tokens: int, scale: float = 0.0, quantized: bool = False, form: str = "auto"):
         assert k_pool.dtype == torch.bfloat16 and v_pool.dtype == torch.bfloat16
         assert block_table.dtype == torch.int32 and seq_lens.dtype == torch.int32
         self.device = k_pool.device
@@ -47,8 +48,8 @@ class LocksRuntime:
         self.cache = L.make_cache(k_pool, v_pool, block_table, seq_lens, self.n_summarized)
         self.summary = L.make_summary(self.basis_t, self.coeffs, rank,
                                       L.LOCKS_DTYPE_Q4 if quantized else L.LOCKS_DTYPE_BF16)
-        self.params = L.make_params(num_q_heads, budget_tokens, scale,
-                                    L.LOCKS_FLAG_UNFUSED if unfused else 0)
+        flags = {"auto": 0, "unfused": L.LOCKS_FLAG_UNFUSED, "fused": L.LOCKS_FLAG_FUSED}[form]
+        self.params = L.make_params(num_q_heads, budget_tokens, scale, flags)
         self.k_max = min(budget_tokens // P, block_table.shape[1])
         self.ws_bytes = L.locks_workspace_size(self.cache, self.summary, self.params)
         self.ws = torch.empty(self.ws_bytes + 256, dtype=torch.uint8, device=self.device)

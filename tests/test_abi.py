@@ -23,7 +23,7 @@ def lib():
 
 def test_library_exports_every_declared_symbol(lib):
     declared = L.declared_symbols()
-    assert len(declared) == 12, declared
+    assert len(declared) == 13, declared
     out = subprocess.run(["nm", "-D", "--defined-only", LIB], capture_output=True, text=True).stdout
     exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
     for name in declared:
@@ -99,7 +99,8 @@ def test_bad_cache_rejected(lib, kw, status):
     (L.make_params(7, 512), L.LOCKS_ERR_INVALID_ARG),      # not a multiple of Hkv
     (L.make_params(34, 512), L.LOCKS_ERR_UNSUPPORTED),     # G = 17
     (L.make_params(8, -1), L.LOCKS_ERR_INVALID_ARG),
-    (L.make_params(8, 512, flags=2), L.LOCKS_ERR_INVALID_ARG),      # a reserved flag bit
+    (L.make_params(8, 512, flags=4), L.LOCKS_ERR_INVALID_ARG),      # a reserved flag bit
+    (L.make_params(8, 512, flags=3), L.LOCKS_ERR_INVALID_ARG),      # both forms requested
     (L.make_params(8, 512, scale=-1.0), L.LOCKS_ERR_INVALID_ARG),
 ])
 def test_bad_params_rejected(lib, params, status):
@@ -160,3 +161,16 @@ def test_product_path_never_imports_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
+
+
+def test_decode_step_launches_validates_its_arguments(lib):
+    """locks_decode_step_launches checks its arguments like the step itself."""
+    cache, summary, params = _cache(), L.make_summary(16, 16, 8), L.make_params(8, 512)
+    with pytest.raises(L.LocksError) as e:
+        L.locks_decode_step_launches(cache, L.make_summary(16, 16, 3), params)
+    assert e.value.status == L.LOCKS_ERR_UNSUPPORTED
+    with pytest.raises(L.LocksError) as e:
+        L.locks_decode_step_launches(cache, summary, L.make_params(7, 512))
+    assert e.value.status == L.LOCKS_ERR_INVALID_ARG
+    # the three-kernel form on request
+    assert L.locks_decode_step_launches(cache, summary, L.make_params(8, 512, flags=L.LOCKS_FLAG_UNFUSED)) == 3

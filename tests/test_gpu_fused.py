@@ -2,9 +2,10 @@
 
 locks_decode_step runs as two kernels (the scan, then attention whose
 thread-block clusters compute the group-shared top-k themselves) for 64-token
-pages with k_max <= 32 and at most 128 pages per CTA of a 16-CTA cluster, and
-as three kernels (scan, top-k, attention) otherwise or with
-LOCKS_FLAG_UNFUSED.  Both forms are checked against the fp64 oracle with the
+pages with k_max <= 32, at most 128 pages per CTA of a 16-CTA cluster and more
+(sequence, KV head) problems than SMs, and as three kernels (scan, top-k,
+attention) otherwise or with LOCKS_FLAG_UNFUSED.  The cases here force the
+two-kernel form with LOCKS_FLAG_FUSED.  Both forms are checked against the fp64 oracle with the
 tolerances of test_gpu_parity (page LSE 1e-3 relative, selection bit-exact
 outside a 1e-4 band around the cut, output 1e-2 absolute, lse 1e-3 relative),
 and against each other: the same pages, and outputs within 1e-2.
@@ -35,12 +36,12 @@ def _built():
     build()
 
 
-def _runtime(case, r, budget, nsum, basis_t, coeffs, unfused):
+def _runtime(case, r, budget, nsum, basis_t, coeffs, form):
     from sparse_kv_page_rank_gb300.runtime import LocksRuntime
     rt = LocksRuntime(to_torch_bf16(case.k_pool, "cuda"), to_torch_bf16(case.v_pool, "cuda"),
                       torch.from_numpy(case.block_table).cuda(), torch.from_numpy(case.seq_lens).cuda(),
                       torch.tensor(np.asarray(nsum, dtype=np.int32)).cuda(), case.num_q_heads, r, budget,
-                      unfused=unfused)
+                      form=form)
     rt.set_summaries(to_torch_bf16(basis_t, "cuda"), to_torch_bf16(coeffs, "cuda"))
     return rt
 
@@ -60,8 +61,8 @@ def _check(case, r, budget, nsum=None, expect_fused=True):
         nsum = [case.n_full_pages(b) for b in range(case.batch)]
     basis_t, coeffs = oracle_summaries_bf16(case, r)
     q = to_torch_bf16(case.q, "cuda")
-    rf = _runtime(case, r, budget, nsum, basis_t, coeffs, unfused=False)
-    ru = _runtime(case, r, budget, nsum, basis_t, coeffs, unfused=True)
+    rf = _runtime(case, r, budget, nsum, basis_t, coeffs, form="fused")
+    ru = _runtime(case, r, budget, nsum, basis_t, coeffs, form="unfused")
     assert rf.decode_step_launches() == (2 if expect_fused else 3)
     assert ru.decode_step_launches() == 3
     fo, fl, fsel, fcnt = _step(rf, q)
@@ -158,11 +159,11 @@ def test_fused_step_llama128k_sampled():
     basis_t, coeffs = _summaries(case, cfg["rank"], heads)
     nsum = [case.n_full_pages(0)]
     q = to_torch_bf16(case.q, "cuda")
-    rf = _runtime(case, cfg["rank"], cfg["budget_tokens"], nsum, basis_t, coeffs, unfused=False)
+    rf = _runtime(case, cfg["rank"], cfg["budget_tokens"], nsum, basis_t, coeffs, form="fused")
     assert rf.decode_step_launches() == 2
     fo, fl, fsel, fcnt = _step(rf, q)
     del rf
-    ru = _runtime(case, cfg["rank"], cfg["budget_tokens"], nsum, basis_t, coeffs, unfused=True)
+    ru = _runtime(case, cfg["rank"], cfg["budget_tokens"], nsum, basis_t, coeffs, form="unfused")
     uo, ul, usel, ucnt = _step(ru, q)
     del ru
     G = case.group
@@ -182,3 +183,16 @@ def test_fused_step_llama128k_sampled():
         assert np.abs(fo[b, hs] - ro[0]).max() <= OUT_ATOL
         assert np.abs(uo[b, hs] - ro[0]).max() <= OUT_ATOL
         assert np.all(np.abs(fl[b, hs] - rl[0]) <= LSE_RTOL * np.maximum(1.0, np.abs(rl[0])))
+
+
+def test_automatic_form_follows_the_problem_count():
+    """Without a flag, the two-kernel form is taken when there are more
+    (sequence, KV head) problems than SMs, and not otherwise."""
+    from sparse_kv_page_rank_gb300.runtime import LocksRuntime
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for batch, expect in ((1, 3), (sms // 8 + 1, 2)):
+        k = torch.zeros((4 * batch, 8, 64, 128), dtype=torch.bfloat16, device="cuda")
+        bt = torch.arange(4 * batch, dtype=torch.int32, device="cuda").view(batch, 4)
+        sl = torch.full((batch,), 256, dtype=torch.int32, device="cuda")
+        rt = LocksRuntime(k, k, bt, sl, torch.full((batch,), 4, dtype=torch.int32, device="cuda"), 32, 8, 128)
+        assert rt.decode_step_launches() == expect, (batch, sms)
