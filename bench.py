@@ -169,15 +169,11 @@ class ClockSampler:
 # reference arm / CPU baseline: the fp64 oracle on a bounded sample
 # ---------------------------------------------------------------------------
 
-def _oracle_sample(case, cfg, kv_heads, budget_seconds: float, steps: int | None = None,
-                   max_pages: int | None = None):
-    """Time the oracle's decode step (summaries precomputed, not timed) on a
-    sample of KV heads of sequence 0, optionally cut to its first
-    ``max_pages`` pages.  The time per (sequence, KV head) problem is scaled
-    by the page ratio (the oracle's cost is linear in the pages it scans) and
-    by the number of problems.  Returns (us per full step, detail)."""
+def _oracle_inputs(case, cfg, kv_heads, max_pages: int | None = None):
+    """One-sequence, one-KV-head slices of sequence 0 for the listed heads,
+    optionally cut to the first ``max_pages`` pages, with the oracle's
+    summaries precomputed (not timed).  Returns (problems, pages, pages_full)."""
     import oracle as O
-    from synth.generator import LocksCase
     r = cfg["rank"]
     G = case.group
     P = case.page_size
@@ -188,36 +184,48 @@ def _oracle_sample(case, cfg, kv_heads, budget_seconds: float, steps: int | None
     n_pages = -(-int(seq_sample[0]) // P)
     phys = case.block_table[b, :n_pages]
     bt = np.arange(n_pages, dtype=np.int32)[None, :]
-    subs = []
+    probs = []
     for h in kv_heads:
-        # one-sequence, one-KV-head slice of the cache on a compact pool, same bf16 inputs
         kp = np.ascontiguousarray(case.k_pool[phys, h:h + 1])
         vp = np.ascontiguousarray(case.v_pool[phys, h:h + 1])
-        sub = LocksCase(batch=1, num_q_heads=G, num_kv_heads=1, head_dim=D, page_size=P,
-                        seq_lens=seq_sample, block_table=bt, k_pool=kp, v_pool=vp,
-                        q=case.q[b:b + 1, h * G:(h + 1) * G], carriers=case.carriers[b:b + 1, h:h + 1],
-                        carrier_heads=case.carrier_heads[b:b + 1, h:h + 1],
-                        outlier_channels=case.outlier_channels, seed=case.seed)
         basis = np.zeros((n_pages, 1, D, r))
         coeffs = np.zeros((n_pages, 1, P, r))
         for j in range(nfull):
             V, C, _, _ = O.page_summary(O.bf16_widen(kp[j, 0]), r)
             basis[j, 0], coeffs[j, 0] = V, C
-        subs.append((sub, basis, coeffs))
+        probs.append(dict(q=np.ascontiguousarray(case.q[b:b + 1, h * G:(h + 1) * G]), kp=kp, vp=vp, bt=bt,
+                          seq=seq_sample, nfull=nfull, basis=basis, coeffs=coeffs,
+                          budget=cfg["budget_tokens"], P=P))
+    return probs, nfull, nfull_all
+
+
+def _oracle_problem(prob) -> float:
+    """Seconds the oracle takes for one (sequence, KV head) decode step."""
+    import oracle as O
+    t0 = time.perf_counter()
+    O.decode_step(prob["q"], prob["kp"], prob["vp"], prob["bt"], prob["seq"], [prob["nfull"]], prob["basis"],
+                  prob["coeffs"], 1, prob["budget"], page_size=prob["P"])
+    return time.perf_counter() - t0
+
+
+def _oracle_sample(case, cfg, kv_heads, budget_seconds: float, steps: int | None = None,
+                   max_pages: int | None = None):
+    """Time the oracle's decode step on one core, problem after problem
+    (sequence 0, the listed KV heads, optionally its first ``max_pages``
+    pages).  The time per (sequence, KV head) problem is scaled by the page
+    ratio (the oracle's cost is linear in the pages it scans) and by the
+    number of problems.  Returns (us per full step, detail)."""
+    probs, nfull, nfull_all = _oracle_inputs(case, cfg, kv_heads, max_pages)
     times = []
     t_end = time.perf_counter() + budget_seconds
     i = 0
     while True:
-        sub, basis, coeffs = subs[i % len(subs)]
-        t0 = time.perf_counter()
-        O.decode_step(sub.q, sub.k_pool, sub.v_pool, sub.block_table, sub.seq_lens, [nfull], basis, coeffs,
-                      1, cfg["budget_tokens"], page_size=P)
-        times.append(time.perf_counter() - t0)
+        times.append(_oracle_problem(probs[i % len(probs)]))
         i += 1
         if steps is not None:
             if i >= steps:
                 break
-        elif time.perf_counter() > t_end and i >= len(subs):
+        elif time.perf_counter() > t_end and i >= len(probs):
             break
     per_problem = statistics.median(times) * (nfull_all / max(nfull, 1))
     full = per_problem * case.batch * case.num_kv_heads
@@ -225,34 +233,76 @@ def _oracle_sample(case, cfg, kv_heads, budget_seconds: float, steps: int | None
                             pages_full=nfull_all)
 
 
+def _oracle_pool():
+    """A pool of os.cpu_count() spawned worker processes (spawned, not forked:
+    safe after the CUDA context exists), warmed up so that timed work excludes
+    interpreter start-up and imports."""
+    import concurrent.futures as cf
+    import multiprocessing as mp
+    cores = os.cpu_count() or 1
+    ex = cf.ProcessPoolExecutor(max_workers=cores, mp_context=mp.get_context("spawn"))
+    list(ex.map(_oracle_warm, range(cores)))
+    return ex, cores
+
+
+def _oracle_warm(_):
+    import oracle  # noqa: F401
+    return 0
+
+
+def _oracle_all_cores(ex, cores, probs, nfull, nfull_all, problems_total, rounds: int = 1):
+    """The oracle problems run on every host core at once (``rounds`` whole
+    problems per core in the pool ``ex``): wall time scaled by pages and to
+    ``problems_total`` problems.  Returns (us per full step, detail)."""
+    work = [probs[i % len(probs)] for i in range(cores * rounds)]
+    t0 = time.perf_counter()
+    list(ex.map(_oracle_problem, work))
+    wall = time.perf_counter() - t0
+    per_problem_wall = wall / len(work) * (nfull_all / max(nfull, 1))
+    return per_problem_wall * problems_total * 1e6, dict(problems=len(work), wall_s=wall, pages=nfull,
+                                                          pages_full=nfull_all)
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    case, cfg = make_config_case(args.config, page_size=args.page_size)
+    case, cfg = make_config_case(args.config, page_size=args.page_size, **_rank_override(args))
     W, K = args.warmup, args.steps
-    # each step: one (sequence, KV head) problem of the workload on a page
-    # window sized so that K + W steps take about two minutes, scaled to a full step
+    cores = os.cpu_count() or 1
+    # each step: every host core runs one (sequence, KV head) problem of the
+    # workload on a page window sized so that K + W steps take about two
+    # minutes, scaled to a full step
     t0 = time.perf_counter()
     _, probe = _oracle_sample(case, cfg, [0], 0.0, steps=1, max_pages=256)
     per_page = probe["times"][0] / max(probe["pages"], 1)
     window = int(max(16, min(case.n_full_pages(0), 120.0 / (K + W) / max(per_page, 1e-9))))
-    _oracle_sample(case, cfg, [0], 0.0, steps=max(W, 1), max_pages=window)
-    us_full, det = _oracle_sample(case, cfg, range(case.num_kv_heads), 0.0, steps=K, max_pages=window)
+    probs, nfull, nfull_all = _oracle_inputs(case, cfg, range(case.num_kv_heads), max_pages=window)
+    ex, cores = _oracle_pool()
+    total = case.batch * case.num_kv_heads
+    for _ in range(W):
+        _oracle_all_cores(ex, cores, probs, nfull, nfull_all, total)
+    vals = [_oracle_all_cores(ex, cores, probs, nfull, nfull_all, total)[0] for _ in range(K)]
+    ex.shutdown()
+    us_full = statistics.median(vals)
     wall = time.perf_counter() - t0
     line = {
         "impl": "reference", "metric": METRIC, "value": us_full, "unit": "us", "n_gpus": args.gpus,
         "steps": K, "warmup": W, "ms_per_step": us_full / 1e3, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": _config_dict(args.config, case, cfg),
-        "cpu_baseline": {"value": us_full, "unit": "us", "cores": 1, "kind": "oracle",
-                         "sample": f"each step = one (sequence, KV head) problem of {args.config} on its first "
-                                   f"{det['pages']} of {det['pages_full']} pages (summaries precomputed), "
-                                   f"median scaled by pages and x {case.batch * case.num_kv_heads} problems; "
-                                   f"{det['problems_timed']} steps, {wall:.1f} s"},
+        "cpu_baseline": {"value": us_full, "unit": "us", "cores": cores, "kind": "oracle",
+                         "sample": f"each step = {cores} (sequence, KV head) problems of {args.config} at once, one "
+                                   f"per host core, on the first {window} of {case.n_full_pages(0)} pages "
+                                   f"(summaries precomputed), wall time scaled by pages and to "
+                                   f"{case.batch * case.num_kv_heads} problems; median of {K} steps, {wall:.1f} s"},
         "e2e": {"value": us_full, "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
+
+
+def _rank_override(args) -> dict:
+    return {"rank": args.rank} if getattr(args, "rank", None) else {}
 
 
 def _config_dict(name, case, cfg, extra=None):
@@ -271,27 +321,21 @@ def _config_dict(name, case, cfg, extra=None):
 # GPU arm
 # ---------------------------------------------------------------------------
 
-def run_gpu(args):
+def _gpu_workload(args, name, K, W, world, dev, *, page_size=P, rank_override=None, full=True):
+    """Draw the named workload, build its summaries with the library's builder
+    and time (each as one CUDA graph of K calls on R rotating cache copies):
+    the decode step, the dense decode and the summary scan alone.  With
+    ``full`` also the end-to-end forms, the quantised format and the clocks.
+    Returns a dict of measurements."""
     import torch
-    import torch.distributed as dist
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        dist.init_process_group("gloo")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-
-    from sparse_kv_page_rank_gb300.build_lib import build
-    build()
-    from sparse_kv_page_rank_gb300 import locks as L
     from sparse_kv_page_rank_gb300.runtime import LocksRuntime
 
-    case, cfg = make_config_case(args.config, page_size=args.page_size)
+    overrides = {"rank": rank_override} if rank_override else {}
+    case, cfg = make_config_case(name, page_size=page_size, **overrides)
     r, budget = cfg["rank"], cfg["budget_tokens"]
     B, Hq, Hkv, G = case.batch, case.num_q_heads, case.num_kv_heads, case.group
-    P = case.page_size
+    Pg = case.page_size
 
     def to_dev(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
@@ -303,12 +347,16 @@ def run_gpu(args):
     ns = torch.from_numpy(nsum_host).to(dev)
     q = torch.from_numpy(case.q.view(np.int16)).view(torch.bfloat16).to(dev)
     pages = torch.from_numpy(np.concatenate([case.block_table[b, :nsum_host[b]] for b in range(B)])).to(dev)
+    carriers = case.carriers.copy()
+    seq_lens = case.seq_lens.copy()
+    config = _config_dict(name, case, cfg)
+    del case
 
-    per_copy = k0.numel() * 4 + (r * D + P * r) * 2 * case.pages_total * Hkv
+    per_copy = k0.numel() * 4 + (r * D + Pg * r) * 2 * k0.shape[0] * Hkv
     # bytes one step touches (summaries + selected pages); rotate enough copies
     # that consecutive replays of the same copy are > 4x L2 apart
-    touched = Hkv * int(nsum_host.sum()) * summary_bytes_per_page_head(r, P) + \
-        B * Hkv * min(budget // P, case.max_pages) * P * D * 4
+    touched = Hkv * int(nsum_host.sum()) * summary_bytes_per_page_head(r, Pg) + \
+        B * Hkv * min(budget // Pg, bt.shape[1]) * Pg * D * 4
     R = max(2, min(16, math.ceil(4 * 129e6 / max(touched, 1))))
     if args.copies:
         R = args.copies
@@ -316,10 +364,7 @@ def run_gpu(args):
     for i in range(R):
         kk = k0 if i == 0 else k0.clone()
         vv = v0 if i == 0 else v0.clone()
-        rt = LocksRuntime(kk, vv, bt, sl, ns, Hq, r, budget)
-        rts.append(rt)
-    del case.k_pool, case.v_pool
-    # summaries by the library's builder (timed once, outside the step)
+        rts.append(LocksRuntime(kk, vv, bt, sl, ns, Hq, r, budget))
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
@@ -327,14 +372,13 @@ def run_gpu(args):
     e1.record()
     torch.cuda.synchronize()
     build_ms = e0.elapsed_time(e1)
-    build_pages_per_s = pages.numel() * Hkv / (build_ms / 1e3)
     for rt in rts[1:]:
         rt.set_summaries(rts[0].basis_t, rts[0].coeffs)
     torch.cuda.synchronize()
     assert rts[0].device_error() == 0
 
     stream = torch.cuda.Stream(device=dev)
-    page_lse_bufs = [torch.empty((B, Hq, case.max_pages), dtype=torch.float32, device=dev) for _ in rts]
+    page_lse_bufs = [torch.empty((B, Hq, bt.shape[1]), dtype=torch.float32, device=dev) for _ in rts]
 
     def capture(fn, nsteps):
         """One CUDA graph holding `nsteps` consecutive calls, step i on copy
@@ -362,6 +406,7 @@ def run_gpu(args):
             gw.replay()
         stream.synchronize()
         if world > 1:
+            import torch.distributed as dist
             dist.barrier()
         torch.cuda.synchronize()
         s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -386,54 +431,70 @@ def run_gpu(args):
     step_fn = lambda i, rt: rt.decode_step(q, stream=stream)  # noqa: E731
     dense_fn = lambda i, rt: rt.dense_decode(q, rt.out, rt.lse, stream=stream)  # noqa: E731
     scan_fn = lambda i, rt: rt.page_scores(q, page_lse_bufs[i], stream=stream)  # noqa: E731
-
-    K, W = args.steps, max(3, args.warmup)
+    res = dict(config=config, R=R, per_copy=per_copy, r=r, budget=budget, B=B, Hq=Hq, Hkv=Hkv, G=G, P=Pg,
+               build_ms=build_ms, page_heads_built=int(pages.numel() * Hkv), launches=rts[0].decode_step_launches())
     if args.profile:
-        # a few replays of the step and of the dense decode, nothing else
+        # a few replays of the step, the dense decode and the scan, nothing else
         # (the command ncu captures)
         timed(step_fn, K, W)
         timed(dense_fn, K, W)
         timed(scan_fn, K, W)
         if r <= 8 and not args.no_q4:
-            # the quantised format's step and scan, after the bf16 ones
             qrts = [LocksRuntime(rt_.k_pool, rt_.v_pool, bt, sl, ns, Hq, r, budget, quantized=True) for rt_ in rts]
             qrts[0].build_summaries(pages)
             for qrt in qrts[1:]:
                 qrt.set_summaries(qrts[0].basis_t, None)
             timed(lambda i, rt_: qrts[i].decode_step(q, stream=stream), K, W)
             timed(lambda i, rt_: qrts[i].page_scores(q, page_lse_bufs[i], stream=stream), K, W)
-        print(json.dumps({"profile": args.config, "copies": R, "steps": K, "warmup": W}))
-        return
-    clocks = ClockSampler(local)
+        return res
+
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
     clocks.start()
     time.sleep(0.3)
     step_ms = timed(step_fn, K, W, extra_replays=9)
-    step_pct = {f"p{p}": float(np.percentile(np.array([step_ms] + replay_ms) * 1e3, p)) for p in (10, 50, 90)}
-    clk = clocks.stop()
-    dense_ms = timed(dense_fn, max(20, K // 4), W)
-    scan_ms = timed(scan_fn, K, W)
+    res["step_ms"] = step_ms
+    res["step_pct"] = {f"p{p}": float(np.percentile(np.array([step_ms] + replay_ms) * 1e3, p)) for p in (10, 50, 90)}
+    res["clocks"] = clocks.stop()
+    res["dense_ms"] = timed(dense_fn, max(20, K // 4), W)
+    res["scan_ms"] = timed(scan_fn, K, W)
 
-    # e2e through the public API: pinned host q -> device, decode step, out -> pinned host
-    q_host = q.cpu().pin_memory()
-    out_host = torch.empty((B, Hq, D), dtype=torch.bfloat16).pin_memory()
-    q_dev = torch.empty_like(q)
+    if full:
+        # end to end through the public API, pinned host q in, pinned host out
+        q_host = q.cpu().pin_memory()
+        out_host = torch.empty((B, Hq, D), dtype=torch.bfloat16).pin_memory()
+        q_dev = torch.empty_like(q)
 
-    def e2e_zero_copy_fn(i, rt):
-        # the kernels read q from, and write out to, page-locked host memory
-        rt.decode_step(q_host, out=out_host, stream=stream)
+        def e2e_zero_copy_fn(i, rt):
+            # the kernels read q from, and write out to, page-locked host memory
+            rt.decode_step(q_host, out=out_host, stream=stream)
 
-    def e2e_fn(i, rt):
-        q_dev.copy_(q_host, non_blocking=True)
-        rt.decode_step(q_dev, stream=stream)
-        out_host.copy_(rt.out, non_blocking=True)
+        def e2e_fn(i, rt):
+            q_dev.copy_(q_host, non_blocking=True)
+            rt.decode_step(q_dev, stream=stream)
+            out_host.copy_(rt.out, non_blocking=True)
 
-    e2e_ms_copy = timed(e2e_fn, K, W)
-    e2e_ms_dev = timed(e2e_zero_copy_fn, K, W)
+        res["e2e_copy_ms"] = timed(e2e_fn, K, W)
+        res["e2e_dev_ms"] = timed(e2e_zero_copy_fn, K, W)
+        # one step as a caller sees it: replay a one-step graph (q copied in,
+        # the step, out copied back), wait for the stream, read the output on
+        # the host; host clock around each call
+        g1 = capture(e2e_fn, 1)
+        host_us = []
+        for it in range(300):
+            t0 = time.perf_counter()
+            with torch.cuda.stream(stream):
+                g1.replay()
+            stream.synchronize()
+            _ = out_host[0, 0, 0].item()
+            host_us.append((time.perf_counter() - t0) * 1e6)
+        res["e2e_host_us"] = {f"p{p}": float(np.percentile(np.array(host_us[20:]), p)) for p in (10, 50, 90)}
+        res["io_bytes"] = (int(q.numel() * 2), int(B * Hq * D * 2))
+        del g1
     # every timed call must have finished without a device-side error
     # (a bounded wait that ran out, or a bad block-table entry)
     errs = [rt_.device_error() for rt_ in rts]
     if any(errs):
-        raise SystemExit(f"device error bits {errs} after the timed steps: this run is invalid")
+        raise SystemExit(f"device error bits {errs} after the timed steps of {name}: this run is invalid")
 
     # quality: mass recall of the selected pages against the exact page LSE
     # (read-every-key, on the GPU), and carrier retention
@@ -460,16 +521,18 @@ def run_gpu(args):
             best = np.lexsort((np.arange(n), -sig))[:k]
             oracle_recalls.append(float(np.mean(np.exp(np.logaddexp.reduce(s_star[:, best], axis=1) - tot))))
             cs = set(chosen.tolist())
-            for cpg in case.carriers[b, h]:
+            for cpg in carriers[b, h]:
                 if cpg >= 0:
                     total += 1
                     kept += int(cpg) in cs
     assert rt.device_error() == 0
+    res.update(mass_recall=float(np.mean(recalls)), exact_lse_selection_recall=float(np.mean(oracle_recalls)),
+               carrier_retention=kept / total if total else None)
 
     # The quantised, centred summary format (int4 basis, int8 coefficients and
     # centroid) on the same caches: its builder, step and scan.
-    q4 = None
-    if r <= 8 and not args.no_q4:
+    res["q4"] = None
+    if full and r <= 8 and not args.no_q4:
         from sparse_kv_page_rank_gb300.locks import q4_page_head_bytes
         qrts = [LocksRuntime(rt_.k_pool, rt_.v_pool, bt, sl, ns, Hq, r, budget, quantized=True) for rt_ in rts]
         torch.cuda.synchronize()
@@ -498,81 +561,145 @@ def run_gpu(args):
                 chosen = qsel[b, h, :qcnt[b, h]]
                 qrec.append(float(np.mean(np.exp(np.logaddexp.reduce(s_star[:, chosen], axis=1) - tot))))
                 cs = set(chosen.tolist())
-                qkept += sum(int(cpg) in cs for cpg in case.carriers[b, h] if cpg >= 0)
-        qb = q4_page_head_bytes(r, P)
+                qkept += sum(int(cpg) in cs for cpg in carriers[b, h] if cpg >= 0)
+        qb = q4_page_head_bytes(r, Pg)
         q_scan_alg = Hkv * int(nsum_host.sum()) * (qb + G * 4)
         q_traffic = None
-        if (args.config, P) in SCAN_Q4_TRAFFIC_PER_PAGE_HEAD and SCAN_TRAFFIC_SOURCE_SHA == _scan_source_sha():
-            q_traffic = SCAN_Q4_TRAFFIC_PER_PAGE_HEAD[(args.config, P)] * Hkv * int(nsum_host.sum())
-        q4 = {"value": q4_step_ms * 1e3, "unit": "us", "summary_bytes_per_page_head": qb,
-              "residency": qb / (2 * P * D * 2), "speedup_vs_dense": dense_ms / q4_step_ms,
-              "scan_us": q4_scan_ms * 1e3, "scan_gbs": q_scan_alg / (q4_scan_ms * 1e-3) / 1e9,
-              "scan_algorithmic_bytes": q_scan_alg, "scan_traffic": q_traffic,
-              "mass_recall": float(np.mean(qrec)), "carrier_retention": qkept / total if total else None,
-              "summary_build": {"pages_per_s": pages.numel() * Hkv / (q4_build_ms / 1e3), "ms": q4_build_ms},
-              "format": "centred; int4 basis, int8 coefficients and centroid, float32 scales per vector"}
+        if (name, Pg) in SCAN_Q4_TRAFFIC_PER_PAGE_HEAD and SCAN_TRAFFIC_SOURCE_SHA == _scan_source_sha():
+            q_traffic = SCAN_Q4_TRAFFIC_PER_PAGE_HEAD[(name, Pg)] * Hkv * int(nsum_host.sum())
+        res["q4"] = {"value": q4_step_ms * 1e3, "unit": "us", "summary_bytes_per_page_head": qb,
+                     "residency": qb / (2 * Pg * D * 2), "speedup_vs_dense": res["dense_ms"] / q4_step_ms,
+                     "scan_us": q4_scan_ms * 1e3, "scan_gbs": q_scan_alg / (q4_scan_ms * 1e-3) / 1e9,
+                     "scan_algorithmic_bytes": q_scan_alg, "scan_traffic": q_traffic,
+                     "mass_recall": float(np.mean(qrec)), "carrier_retention": qkept / total if total else None,
+                     "summary_build": {"pages_per_s": pages.numel() * Hkv / (q4_build_ms / 1e3), "ms": q4_build_ms},
+                     "format": "centred; int4 basis, int8 coefficients and centroid, float32 scales per vector"}
         del qrts
 
     n_sum_tot = int(nsum_host.sum())
     sb = dict(summaries=0, shat=0, selected_kv=0, qo=0, total=0)
     for b in range(B):
         bb = step_bytes(1, Hkv, G, int(nsum_host[b]), int(cnt[b].mean()),
-                        int(case.seq_lens[b]) - int(nsum_host[b]) * P, r, P)
+                        int(seq_lens[b]) - int(nsum_host[b]) * Pg, r, Pg)
         for key in sb:
             sb[key] += bb[key]
-    db = sum(dense_bytes(1, Hkv, G, int(case.seq_lens[b])) for b in range(B))
-    scan_alg = Hkv * n_sum_tot * (summary_bytes_per_page_head(r, P) + G * 4)
-    peak, peak_kind = _peaks()
-    step_us = step_ms * 1e3
-    eff_gbs = sb["total"] / (step_ms * 1e-3) / 1e9
-    scan_gbs = scan_alg / (scan_ms * 1e-3) / 1e9
-    dense_gbs = db / (dense_ms * 1e-3) / 1e9
-    traffic = None
-    if (args.config, P) in SCAN_TRAFFIC_PER_PAGE_HEAD and SCAN_TRAFFIC_SOURCE_SHA == _scan_source_sha():
-        traffic = SCAN_TRAFFIC_PER_PAGE_HEAD[(args.config, P)] * Hkv * n_sum_tot
+    res["step_bytes"] = sb
+    res["dense_bytes"] = sum(dense_bytes(1, Hkv, G, int(seq_lens[b])) for b in range(B))
+    res["scan_alg"] = Hkv * n_sum_tot * (summary_bytes_per_page_head(r, Pg) + G * 4)
+    res["scan_traffic"] = None
+    if (name, Pg) in SCAN_TRAFFIC_PER_PAGE_HEAD and SCAN_TRAFFIC_SOURCE_SHA == _scan_source_sha() and \
+            r == CONFIGS[name]["rank"]:
+        res["scan_traffic"] = SCAN_TRAFFIC_PER_PAGE_HEAD[(name, Pg)] * Hkv * n_sum_tot
+    del rts
+    torch.cuda.empty_cache()
+    return res
 
-    # CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only)
+
+def _roofline(res, peak, peak_kind):
+    scan_gbs = res["scan_alg"] / (res["scan_ms"] * 1e-3) / 1e9
+    return {"kernel": "scan_kernel (summary scan)", "bound": "hbm", "achieved": scan_gbs, "peak": peak,
+            "unit": "GB/s", "frac": scan_gbs / peak, "traffic": res["scan_traffic"],
+            "peak_kind": f"{peak_kind} (hbm_gbs, burst copy)", "scan_us": res["scan_ms"] * 1e3,
+            "algorithmic_bytes": res["scan_alg"]}
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from sparse_kv_page_rank_gb300.build_lib import build
+    build()
+
+    K, W = args.steps, max(3, args.warmup)
+    res = _gpu_workload(args, args.config, K, W, world, dev, page_size=args.page_size, rank_override=args.rank)
+    if args.profile:
+        print(json.dumps({"profile": args.config, "copies": res["R"], "steps": K, "warmup": W}))
+        return
+    peak, peak_kind = _peaks()
+    step_ms = res["step_ms"]
+    sb = res["step_bytes"]
+    eff_gbs = sb["total"] / (step_ms * 1e-3) / 1e9
+
+    # the 1M-context workload beside the 128K headline (step, dense, scan)
+    ctx1m = None
+    if args.config == "llama128k" and args.page_size == P and not args.rank and not args.no_ctx1m:
+        r1 = _gpu_workload(args, "ctx1m", K, W, world, dev, full=False)
+        e1 = r1["step_bytes"]["total"] / (r1["step_ms"] * 1e-3) / 1e9
+        ctx1m = {"value": r1["step_ms"] * 1e3, "unit": "us", "config": r1["config"],
+                 "step_us_over_replays": r1["step_pct"], "dense_us": r1["dense_ms"] * 1e3,
+                 "speedup_vs_dense": r1["dense_ms"] / r1["step_ms"], "effective_gbs": e1,
+                 "step_frac_of_hbm": e1 / peak, "step_bytes": r1["step_bytes"], "dense_bytes": r1["dense_bytes"],
+                 "kv_bytes_ratio": r1["dense_bytes"] / r1["step_bytes"]["total"],
+                 "mass_recall": r1["mass_recall"], "exact_lse_selection_recall": r1["exact_lse_selection_recall"],
+                 "carrier_retention": r1["carrier_retention"], "roofline": _roofline(r1, peak, peak_kind),
+                 "gpu_launches": r1["launches"] * K, "clocks": r1["clocks"],
+                 "timing": {"l2": f"rotating {r1['R']} independent copies of cache + summaries "
+                                  f"({r1['R'] * r1['per_copy'] / 1e9:.2f} GB > 129 MB L2)"}}
+
+    # CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only), on
+    # one core and on every host core
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        from synth import make_config_case as mk
-        case2, cfg2 = mk(args.config, page_size=P)
-        us_full, det = _oracle_sample(case2, cfg2, range(min(Hkv, 2)), args.cpu_seconds)
-        cpu = {"value": us_full, "unit": "us", "cores": 1, "kind": "oracle",
-               "sample": f"fp64 numpy oracle decode step (summaries precomputed) on KV heads 0-"
-                         f"{min(Hkv, 2) - 1} of sequence 0, {det['problems_timed']} problems in "
-                         f"~{args.cpu_seconds:.0f} s, median per problem x {B * Hkv} problems"}
+        case2, cfg2 = make_config_case(args.config, page_size=args.page_size, **_rank_override(args))
+        heads = range(min(res["Hkv"], 2))
+        us_1, det = _oracle_sample(case2, cfg2, heads, args.cpu_seconds)
+        probs, nfull, nfull_all = _oracle_inputs(case2, cfg2, range(res["Hkv"]), max_pages=256)
+        ex, cores = _oracle_pool()
+        us_all, det_all = _oracle_all_cores(ex, cores, probs, nfull, nfull_all, res["B"] * res["Hkv"], rounds=2)
+        ex.shutdown()
+        cpu = {"value": us_all, "unit": "us", "cores": cores, "kind": "oracle",
+               "sample": f"fp64 numpy oracle decode step (summaries precomputed): {det_all['problems']} (sequence, "
+                         f"KV head) problems of sequence 0, first {det_all['pages']} of {det_all['pages_full']} "
+                         f"pages, on {cores} host cores at once ({det_all['wall_s']:.1f} s wall), scaled by pages "
+                         f"and to {res['B'] * res['Hkv']} problems",
+               "one_core": {"value": us_1, "unit": "us", "cores": 1,
+                            "sample": f"KV heads 0-{min(res['Hkv'], 2) - 1} of sequence 0, {det['problems_timed']} "
+                                      f"problems in ~{args.cpu_seconds:.0f} s, median per problem x "
+                                      f"{res['B'] * res['Hkv']} problems"}}
 
     line = {
-        "metric": METRIC, "value": step_us, "unit": "us", "n_gpus": world, "steps": K, "warmup": W,
-        "ms_per_step": step_ms, "step_us_over_replays": step_pct, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic",
-        "config": _config_dict(args.config, case, cfg, {
-            "l2": f"rotating {R} independent copies of cache + summaries "
-                  f"({R * per_copy / 1e9:.2f} GB > 129 MB L2)",
-            "graph": "one CUDA graph of K consecutive locks_decode_step calls (rotating copies)"}),
+        "metric": METRIC, "value": step_ms * 1e3, "unit": "us", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": step_ms, "step_us_over_replays": res["step_pct"], "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": res["config"],
+        "timing": {"l2": f"rotating {res['R']} independent copies of cache + summaries "
+                         f"({res['R'] * res['per_copy'] / 1e9:.2f} GB > 129 MB L2)",
+                   "graph": "one CUDA graph of K consecutive locks_decode_step calls (rotating copies)"},
         "effective_gbs": eff_gbs,
         "step_frac_of_hbm": eff_gbs / peak,
-        "dense_us": dense_ms * 1e3, "dense_effective_gbs": dense_gbs, "speedup_vs_dense": dense_ms / step_ms,
-        "step_bytes": sb, "dense_bytes": db, "kv_bytes_ratio": db / sb["total"],
-        "residency": residency(r, P), "mass_recall": float(np.mean(recalls)),
-        "exact_lse_selection_recall": float(np.mean(oracle_recalls)),
-        "carrier_retention": kept / total if total else None,
-        "summary_build": {"pages_per_s": build_pages_per_s, "ms": build_ms, "page_heads": int(pages.numel() * Hkv)},
-        "roofline": {"kernel": "scan_kernel (summary scan)", "bound": "hbm", "achieved": scan_gbs,
-                     "peak": peak, "unit": "GB/s", "frac": scan_gbs / peak, "traffic": traffic,
-                     "peak_kind": f"{peak_kind} (hbm_gbs, burst copy)", "scan_us": scan_ms * 1e3,
-                     "algorithmic_bytes": scan_alg},
+        "dense_us": res["dense_ms"] * 1e3, "dense_effective_gbs": res["dense_bytes"] / (res["dense_ms"] * 1e-3) / 1e9,
+        "speedup_vs_dense": res["dense_ms"] / step_ms,
+        "step_bytes": sb, "dense_bytes": res["dense_bytes"], "kv_bytes_ratio": res["dense_bytes"] / sb["total"],
+        "residency": residency(res["r"], res["P"]), "mass_recall": res["mass_recall"],
+        "exact_lse_selection_recall": res["exact_lse_selection_recall"],
+        "carrier_retention": res["carrier_retention"],
+        "summary_build": {"pages_per_s": res["page_heads_built"] / (res["build_ms"] / 1e3), "ms": res["build_ms"],
+                          "page_heads": res["page_heads_built"]},
+        "roofline": _roofline(res, peak, peak_kind),
         "cpu_baseline": cpu,
-        "e2e": {"value": e2e_ms_dev * 1e3, "unit": "us", "h2d_bytes_per_step": int(q.numel() * 2),
-                "d2h_bytes_per_step": int(B * Hq * D * 2),
+        "e2e": {"value": res["e2e_dev_ms"] * 1e3, "unit": "us", "h2d_bytes_per_step": res["io_bytes"][0],
+                "d2h_bytes_per_step": res["io_bytes"][1],
                 "how": "per step inside one CUDA graph: locks_decode_step reads q from and writes out to "
                        "page-locked host memory in place (the kernels move the data over the CPU-GPU link)",
-                "memcpy_value": e2e_ms_copy * 1e3,
+                "memcpy_value": res["e2e_copy_ms"] * 1e3,
                 "memcpy_how": "the same with cudaMemcpyAsync of q (pinned host -> device) before and of out "
-                              "(device -> pinned host) after each step"},
-        "q4": q4,
-        "gpu_launches": rts[0].decode_step_launches() * K,
-        "clocks": clk,
+                              "(device -> pinned host) after each step",
+                "host_clocked_us": res["e2e_host_us"],
+                "host_clocked_how": "one step as a caller sees it: replay of a one-step graph (q copied in, the "
+                                    "step, out copied back), stream synchronise, out read on the host; host clock "
+                                    "around each of 280 calls"},
+        "q4": res["q4"],
+        "ctx1m": ctx1m,
+        "gpu_launches": res["launches"] * K,
+        "clocks": res["clocks"],
     }
     if rank == 0:
         print(json.dumps(line))
@@ -773,6 +900,8 @@ def main():
     ap.add_argument("--growing-segments", type=int, default=6, help="64-step segments in the growing loop")
     ap.add_argument("--batch-sweep", action="store_true", help="batched throughput at 256K context")
     ap.add_argument("--batches", type=int, nargs="+", default=[8, 32, 64])
+    ap.add_argument("--rank", type=int, default=0, help="summary rank (0 = the workload's own)")
+    ap.add_argument("--no-ctx1m", action="store_true", help="skip the 1M-context sub-measurement")
     args = ap.parse_args()
     if args.batch_sweep:
         run_batch_sweep(args)
