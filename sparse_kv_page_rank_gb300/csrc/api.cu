@@ -33,7 +33,7 @@ int device_sm_count() {
 struct Plan {
   bool ok = true;  // false: shapes beyond what the launch plan supports
   int G = 0, Hq = 0, BH = 0, k_max = 0;
-  int scan_chunk = 0, n_scan = 0;
+  int scan_chunk = 0, n_scan = 0, scan_hg = 1;
   int tk_chunk = 0, n_tk = 0;
   size_t tk_keys = 0;
   int sparse_cluster = 1, dense_cluster = 1, dense_nc = 1, lse_splits = 1;
@@ -101,12 +101,16 @@ Plan make_plan(const locks_cache_t* c, const locks_params_t* p) {
   const int ppt = kPage / P;
   const long long max_tiles = (c->max_pages + ppt - 1) / ppt;
 
-  // scan: about two resident CTAs per SM, pages per CTA a multiple of the warp count
+  // scan: one CTA per SM, each over a range of pages of one sequence for a
+  // block of HG KV heads.  Every (sequence, head block) gets the same number
+  // of chunks, at most SMs / blocks of them, so that all CTAs fit in one wave
+  // (rounding the chunk size up instead can leave a few full-length CTAs for
+  // a second wave, which doubles the scan)
   {
-    const long long target = 2LL * sms;
-    long long per = (BH * c->max_pages + target - 1) / target;
-    per = std::max<long long>(kScanWarps, (per + kScanWarps - 1) / kScanWarps * kScanWarps);
-    pl.scan_chunk = (int)std::min<long long>(per, (long long)c->max_pages + kScanWarps);
+    pl.scan_hg = scan_heads_per_block(c->num_kv_heads);
+    const long long blocks = (long long)c->batch * (c->num_kv_heads / pl.scan_hg);
+    const long long chunks = std::max<long long>(1, std::min<long long>(sms / blocks, c->max_pages));
+    pl.scan_chunk = (int)((c->max_pages + chunks - 1) / chunks);
     pl.n_scan = (c->max_pages + pl.scan_chunk - 1) / pl.scan_chunk;
   }
   // top-k: each CTA scores a fixed chunk of pages (its threads hold the
@@ -272,6 +276,8 @@ locks_status_t run_select(const locks_cache_t* c, const locks_summary_t* s, cons
   sa.scale_log2 = scale_of(p) * kLog2e;
   sa.q4 = s->dtype == LOCKS_DTYPE_Q4 ? 1 : 0;
   sa.page_size = c->page_size;
+  sa.heads_per_block = pl.scan_hg;
+  sa.slots = sa.slot_bytes = sa.basis_bytes = sa.coef_bytes = 0;  // set by the launcher
   cudaError_t e = launch_scan(sa, st, true);
   if (e != cudaSuccess) return LOCKS_ERR_CUDA;
   if (!sel) return LOCKS_OK;  // scan only

@@ -24,6 +24,9 @@ struct ScanArgs {
   float scale_log2;            // scale * log2(e)
   int q4;                      // 1: basis_t holds LOCKS_DTYPE_Q4 blocks (coeffs unused)
   int page_size;               // P: 64 or 16
+  int heads_per_block;         // HG: KV heads one CTA scans together (a power of two dividing Hkv, <= 4)
+  // set by the launcher: ring of `slots` slots, one page of the head block each
+  int slots, slot_bytes, basis_bytes, coef_bytes;
 };
 
 // GSA scores + top-k (chunk-local candidates, merged by the last CTA).
@@ -109,9 +112,15 @@ int topk_pages_per_cta(int group);  // pages one top-k CTA scores
 int attend_max_cluster(int mode, int page_size);  // largest placeable cluster (<= 16) for that mode
                                                   // (kAttendFused: page_size 64 only)
 int attend_active_clusters(int mode, int cs, int page_size);  // clusters of cs CTAs resident at once
-// Scan CTA: 7 consumer warps + 1 producer warp, so that two CTAs put four
-// warps on each SM sub-partition (whose register file is a quarter of the SM's).
-constexpr int kScanWarps = 7;
+// Scan CTA (one per SM): 16 consumer warps + 1 producer warp.
+constexpr int kScanWarps = 16;
+// KV heads one scan CTA covers: the largest power of two <= 4 dividing Hkv
+// (measured on GB300: 4 beats 8 at 128K context and ties elsewhere).
+inline int scan_heads_per_block(int num_kv_heads) {
+  int hg = 4;
+  while (num_kv_heads % hg) hg /= 2;
+  return hg;
+}
 constexpr int kScanThreads = (kScanWarps + 1) * 32;
 constexpr int kTopkThreads = 512;
 constexpr int kAttendThreads = 128;

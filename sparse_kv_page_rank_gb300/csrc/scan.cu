@@ -10,14 +10,20 @@
 // dominant byte stream of the decode step, so it is built to keep HBM busy.
 //
 // Memory (warp-specialised): each CTA owns a contiguous range of pages of one
-// (sequence, KV head) and a ring of S page-head slots in shared memory.  One
-// producer warp keeps the ring full: each of its lanes owns slots, waits for
-// the slot to be released, and issues two TMA bulk copies (the basis block,
-// r rows of 256 bytes, and the coefficient block, P x r), completing on the
-// slot's "full" mbarrier.  Seven consumer warps only compute: consumer w takes
-// pages w, w + 7, ..., waits on the slot's full barrier and releases it on its
-// "empty" barrier.  Up to S page-heads (96 KiB) per CTA are in flight,
-// independent of how long the consumers take per page.
+// sequence for a block of HG KV heads (HG the largest power of two <= 4
+// dividing the KV-head count), and a ring of S slots in shared memory, one
+// page of the block per slot.  The summaries of a physical page are laid out
+// head after head, so a page's bases for all HG heads are one contiguous
+// range and so are its coefficients: one producer warp fills a slot with two
+// TMA bulk copies (one for the quantised format) per page and head block.
+// The copy count, not the bytes, limits a TMA read of small pieces (about
+// 40 ns per copy per SM measured on GB300, whatever the size up to ~1 KiB), so
+// covering HG page-heads per copy is what lets the scan stream at HBM speed.
+// Each of the producer's lanes owns a slot, waits for it to be released and
+// refills it, completing on the slot's "full" mbarrier.  Sixteen consumer
+// warps only compute: warp w serves head w mod HG of the block and every
+// (16 / HG)-th page; it waits on the slot's full barrier and arrives on the
+// slot's "empty" barrier, which completes when all HG heads are done.
 //
 // Compute: one consumer warp per page-head, all G <= 16 heads of the group at
 // once, two bf16 tensor-core contractions:
@@ -47,19 +53,17 @@ namespace locks {
 
 namespace {
 
-// The slot count is a multiple of the consumer-warp count: page p goes to slot
-// p mod kSlots and to warp p mod kScanWarps, so every slot is always consumed
-// by the same warp, which therefore waits on the slot's phases strictly in
-// order.  (With a slot shared by several warps, a warp could wait on the
-// parity of a slot's next phase while the current one is still incomplete;
-// a parity wait on a phase two ahead returns at once, on stale data.)
-template <bool R16, bool Q4 = false>
-struct Ring {
-  static constexpr int kSlots = R16 ? 2 * kScanWarps : 4 * kScanWarps;  // page-heads in flight per CTA
-  static constexpr int kCoef = R16 ? 4096 : 2048;  // basis block (r rows x 256 B) comes first
-  // quantised: one packed block per page-head (rank <= 8)
-  static constexpr int kSlot = Q4 ? LOCKS_Q4_PAGE_HEAD_BYTES(8) : (R16 ? 6144 : 3072);
-};
+// The slot count S is a multiple of the number of warp groups (16 / HG):
+// page p goes to slot p mod S and to the warps of group p mod (16 / HG), so
+// every slot is always consumed by the same warps, which therefore wait on the
+// slot's phases strictly in order.  (With a slot shared by several groups, a
+// warp could wait on the parity of a slot's next phase while the current one
+// is still incomplete; a parity wait on a phase two ahead returns at once, on
+// stale data.)
+constexpr int kMaxSlots = 32;  // one producer lane per slot
+// ring bytes: one CTA per SM; the quantised format also stages centroid data
+constexpr int kRingBytes = 200 * 1024;
+constexpr int kRingBytesQ4 = 176 * 1024;
 
 // Quantised format: q . mu is computed for kMuBatch pages of a warp at once
 // (one MMA tile, a page per column) instead of page by page; each warp
@@ -69,9 +73,27 @@ constexpr int kStageMu = kScanWarps * kMuBatch * 128;        // centroid codes
 constexpr int kStageSmu = kScanWarps * kMuBatch * 4;         // centroid scales
 constexpr int kStagePend = kScanWarps * kMuBatch * 16 * 4;   // base-2 LSE per head row
 
-template <bool R16, bool Q4 = false>
-constexpr int scan_smem_bytes() {
-  return Ring<R16, Q4>::kSlots * Ring<R16, Q4>::kSlot + 1024 + (Q4 ? kStageMu + kStageSmu + kStagePend : 0);
+// Layout of one slot (a page of a head block) and the ring for these shapes.
+struct SlotLayout {
+  int basis_bytes;  // per page-head: r rows of 256 B (quantised: the whole packed block)
+  int coef_bytes;   // per page-head: P x r bf16 (quantised: 0)
+  int slot_bytes;   // HG page-heads
+  int slots;
+  int smem;         // dynamic shared memory of the kernel
+};
+
+SlotLayout slot_layout(int rank, int page_size, int hg, bool q4) {
+  SlotLayout L;
+  L.basis_bytes = q4 ? LOCKS_Q4_BLOCK_BYTES(rank, page_size) : rank * kHeadDim * 2;
+  L.coef_bytes = q4 ? 0 : page_size * rank * 2;
+  L.slot_bytes = hg * (L.basis_bytes + L.coef_bytes);
+  const int groups = kScanWarps / hg;
+  int s = (q4 ? kRingBytesQ4 : kRingBytes) / L.slot_bytes;
+  s = s < kMaxSlots ? s : kMaxSlots;
+  s -= s % groups;
+  L.slots = s;
+  L.smem = s * L.slot_bytes + 128 + (q4 ? kStageMu + kStageSmu + kStagePend : 0);
+  return L;
 }
 
 // x -> hi + lo, each term a bf16 (truncated; the two keep about 16 bits of
@@ -134,17 +156,14 @@ __device__ __forceinline__ float lse2_lanes(float* v) {
 // Page-head in shared memory at `slot` -> base-2 LSE for head g (e0) and,
 // with G16, head g + 8 (e1).
 template <bool G16, bool R16, bool GRP2, int P>
-__device__ __forceinline__ void compute_page(uint32_t slot, const uint4 (&qa)[4], const uint4 (&qb)[4], int r,
-                                             float scale_log2, int lane, float& e0, float& e1) {
-  using RG = Ring<R16>;
+__device__ __forceinline__ void compute_page(uint32_t bas, uint32_t coef, const uint4 (&qa)[4], const uint4 (&qb)[4],
+                                             int r, float scale_log2, int lane, float& e0, float& e1) {
   constexpr int NT = P / 8;  // 8-token n-tiles of the page
   const int g = lane >> 2, c = lane & 3;
   const uint4 z4 = make_uint4(0, 0, 0, 0);
   // basis row `row`, 16-byte piece d = 32*s + 8c (linear rows of 256 B)
-  auto basis_piece = [&](int row, int s) -> uint32_t { return slot + row * 256 + s * 64 + c * 16; };
-  auto coef_word = [&](int jt, int k0) -> uint32_t {
-    return slot + RG::kCoef + (uint32_t)(((8 * jt + g) * r + k0) * 2);
-  };
+  auto basis_piece = [&](int row, int s) -> uint32_t { return bas + row * 256 + s * 64 + c * 16; };
+  auto coef_word = [&](int jt, int k0) -> uint32_t { return coef + (uint32_t)(((8 * jt + g) * r + k0) * 2); };
 
   // (1) W^T = Q V  (16 heads x 8 or 16 basis vectors); two accumulators per
   // n-tile halve the dependent MMA chain
@@ -351,25 +370,26 @@ __device__ __forceinline__ void mu_batch(uint32_t stage_mu, int nb, const uint4 
 }
 
 template <bool G16, bool R16, bool GRP2, bool Q4, int P>
-__global__ void __launch_bounds__(kScanThreads, 2) scan_kernel(const ScanArgs a) {
-  using RG = Ring<R16, Q4>;
-  constexpr int S = RG::kSlots;
-  static_assert(S <= 32 && S % kScanWarps == 0, "one producer lane per slot; one consumer warp per slot");
+__global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(const ScanArgs a) {
   extern __shared__ uint8_t ring_raw[];
   __shared__ float2 red[kScanWarps][16];
-  __shared__ __align__(8) uint64_t full_bar[S], empty_bar[S];
-  __shared__ int slot_ok[S];
+  __shared__ __align__(8) uint64_t full_bar[kMaxSlots], empty_bar[kMaxSlots];
+  __shared__ int slot_ok[kMaxSlots];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
-  const int bh = blockIdx.y, chunk = blockIdx.x;
-  const int b = bh / a.num_kv_heads, hkv = bh % a.num_kv_heads;
+  const int HG = a.heads_per_block, S = a.slots;
+  const int ngrp = kScanWarps / HG;  // warp groups; each group serves every HG head of its pages
+  const int nhb = a.num_kv_heads / HG;
+  const int hblk = blockIdx.y, chunk = blockIdx.x;
+  const int b = hblk / nhb, h0 = (hblk % nhb) * HG;
   const int G = a.group, r = a.rank;
-  const uint32_t ring = (smem_u32(ring_raw) + 1023u) & ~1023u;
+  const uint32_t ring = (smem_u32(ring_raw) + 127u) & ~127u;
+  const uint32_t slot_bytes = (uint32_t)a.slot_bytes;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], 1);
+      mbar_init(&empty_bar[s], (uint32_t)HG);  // one arrival per head of the block
     }
     fence_mbar_init();
   }
@@ -399,8 +419,7 @@ __global__ void __launch_bounds__(kScanThreads, 2) scan_kernel(const ScanArgs a)
     // Each lane tests its own slot without blocking, so a released slot is
     // refilled at once whatever the other lanes' slots are doing.
     const int32_t* bt = a.block_table + (size_t)b * a.max_pages;
-    const size_t ph_stride_b = (size_t)r * kHeadDim, ph_stride_c = (size_t)P * r;
-    const uint32_t basis_bytes = (uint32_t)(r * kHeadDim * 2), coef_bytes = (uint32_t)(P * r * 2);
+    const uint32_t bb = (uint32_t)(HG * a.basis_bytes), cb = (uint32_t)(HG * a.coef_bytes);
     // the block-table entries of this lane's first kPre pages, read up front
     constexpr int kPre = 8;
     int pre[kPre];
@@ -427,18 +446,13 @@ __global__ void __launch_bounds__(kScanThreads, 2) scan_kernel(const ScanArgs a)
         const bool valid = phys >= 0 && phys < a.pages_total;
         slot_ok[lane] = valid ? 1 : 0;
         if (valid) {
-          const size_t ph = (size_t)phys * a.num_kv_heads + hkv;
-          const uint32_t slot = ring + lane * RG::kSlot;
-          if (Q4) {
-            // one packed block per page-head
-            const uint32_t qbytes = (uint32_t)LOCKS_Q4_BLOCK_BYTES(r, P);
-            mbar_arrive_expect_tx(&full_bar[lane], qbytes);
-            bulk_load(slot, reinterpret_cast<const uint8_t*>(a.basis_t) + ph * qbytes, qbytes, &full_bar[lane]);
-          } else {
-            mbar_arrive_expect_tx(&full_bar[lane], basis_bytes + coef_bytes);
-            bulk_load(slot, a.basis_t + ph * ph_stride_b, basis_bytes, &full_bar[lane]);
-            bulk_load(slot + RG::kCoef, a.coeffs + ph * ph_stride_c, coef_bytes, &full_bar[lane]);
-          }
+          // page-heads (phys, h0 .. h0 + HG - 1) are consecutive in both arrays
+          const size_t ph = (size_t)phys * a.num_kv_heads + h0;
+          const uint32_t slot = ring + lane * slot_bytes;
+          mbar_arrive_expect_tx(&full_bar[lane], bb + cb);
+          bulk_load(slot, reinterpret_cast<const uint8_t*>(a.basis_t) + ph * a.basis_bytes, bb, &full_bar[lane]);
+          if (!Q4)
+            bulk_load(slot + bb, reinterpret_cast<const uint8_t*>(a.coeffs) + ph * a.coef_bytes, cb, &full_bar[lane]);
         } else {
           mbar_arrive(&full_bar[lane]);
         }
@@ -446,7 +460,10 @@ __global__ void __launch_bounds__(kScanThreads, 2) scan_kernel(const ScanArgs a)
       }
     }
   } else {
-    // ---- consumers
+    // ---- consumers: warp `warp` serves head hw of the block on the pages of
+    // its group
+    const int hw = warp % HG, grp = warp / HG;
+    const int hkv = h0 + hw, bh = b * a.num_kv_heads + hkv;
     const int Hq = a.num_kv_heads * G;
     uint4 qa[4], qb[4];
     {
@@ -465,10 +482,15 @@ __global__ void __launch_bounds__(kScanThreads, 2) scan_kernel(const ScanArgs a)
                     : make_uint4(0, 0, 0, 0);
       }
     }
+    // this head's basis (or packed block) and coefficients in slot s
+    auto head_basis = [&](int s) -> uint32_t { return ring + s * slot_bytes + hw * a.basis_bytes; };
+    auto head_coef = [&](int s) -> uint32_t {
+      return ring + s * slot_bytes + HG * a.basis_bytes + hw * a.coef_bytes;
+    };
     unsigned long long cyc_wait = 0, cyc_comp = 0;
     // quantised format: this warp's pending pages (centroid codes, centroid
     // scales and base-2 LSEs per head row), flushed kMuBatch at a time
-    const uint32_t stage_end = ring + RG::kSlots * RG::kSlot;
+    const uint32_t stage_end = ring + S * slot_bytes;
     const uint32_t st_mu = stage_end + (uint32_t)(warp * kMuBatch * 128);
     float* st_smu = reinterpret_cast<float*>(ring_raw + (stage_end - smem_u32(ring_raw)) + kStageMu) + warp * kMuBatch;
     float* st_pend = reinterpret_cast<float*>(ring_raw + (stage_end - smem_u32(ring_raw)) + kStageMu + kStageSmu) +
@@ -484,7 +506,7 @@ __global__ void __launch_bounds__(kScanThreads, 2) scan_kernel(const ScanArgs a)
         const int nn = 2 * c + hh;
         if (nn < nb && ((vmask >> nn) & 1u)) {
           const float sm = st_smu[nn] * a.scale_log2;
-          const int j = j0 + warp + kScanWarps * (kdone + nn);
+          const int j = j0 + grp + ngrp * (kdone + nn);
           const float v0 = st_pend[nn * 16 + g] + u[hh] * sm;
           lse2_merge(zm0, zl0, v0, 1.f);
           float v1 = 0.f;
@@ -507,7 +529,7 @@ __global__ void __launch_bounds__(kScanThreads, 2) scan_kernel(const ScanArgs a)
       npend = 0;
       vmask = 0;
     };
-    for (int p = warp; p < n; p += kScanWarps) {
+    for (int p = grp; p < n; p += ngrp) {
       const int s = p % S;
       const unsigned long long t0 = trace_clock();
       const bool ok = mbar_wait(&full_bar[s], (uint32_t)((p / S) & 1));
@@ -520,15 +542,15 @@ __global__ void __launch_bounds__(kScanThreads, 2) scan_kernel(const ScanArgs a)
       float e0 = 0.f, e1 = 0.f;
       if (valid) {
         if (Q4)
-          compute_page_q4<G16, GRP2, P>(ring + s * RG::kSlot, qa, qb, r, a.scale_log2, lane, e0, e1);
+          compute_page_q4<G16, GRP2, P>(head_basis(s), qa, qb, r, a.scale_log2, lane, e0, e1);
         else
-          compute_page<G16, R16, GRP2, P>(ring + s * RG::kSlot, qa, qb, r, a.scale_log2, lane, e0, e1);
+          compute_page<G16, R16, GRP2, P>(head_basis(s), head_coef(s), qa, qb, r, a.scale_log2, lane, e0, e1);
       }
       if (Q4 && valid) {
         // stage the centroid codes (one word per lane), its scale and the LSEs
-        const uint32_t slot = ring + s * RG::kSlot;
-        sts32(st_mu + 128 * npend + 4 * lane, lds32(slot + 64 * r + 4 * lane));
-        if (lane == 0) st_smu[npend] = __uint_as_float(lds32(slot + 64 * r + kHeadDim + P * r + 8 * r));
+        const uint32_t blk = head_basis(s);
+        sts32(st_mu + 128 * npend + 4 * lane, lds32(blk + 64 * r + 4 * lane));
+        if (lane == 0) st_smu[npend] = __uint_as_float(lds32(blk + 64 * r + kHeadDim + P * r + 8 * r));
         if (c == 0) {
           st_pend[npend * 16 + g] = e0;
           if (G16) st_pend[npend * 16 + g + 8] = e1;
@@ -540,12 +562,12 @@ __global__ void __launch_bounds__(kScanThreads, 2) scan_kernel(const ScanArgs a)
       cyc_comp += trace_clock() - t1;
       if (Q4) {
         vmask |= (valid ? 1u : 0u) << npend;
-        if (!valid && lane == 0) set_error(a.err, LOCKS_DEVERR_BLOCK_TABLE);
+        if (!valid && lane == 0 && hw == 0) set_error(a.err, LOCKS_DEVERR_BLOCK_TABLE);
         if (++npend == kMuBatch) flush(kMuBatch);
         continue;
       }
       if (!valid) {
-        if (lane == 0) set_error(a.err, LOCKS_DEVERR_BLOCK_TABLE);
+        if (lane == 0 && hw == 0) set_error(a.err, LOCKS_DEVERR_BLOCK_TABLE);
         continue;
       }
       const int j = j0 + p;
@@ -574,7 +596,7 @@ __global__ void __launch_bounds__(kScanThreads, 2) scan_kernel(const ScanArgs a)
     if (lane == 0) {
       trace_add(a.err, kTrScanCycWait, cyc_wait);
       trace_add(a.err, kTrScanCycCompute, cyc_comp);
-      trace_add(a.err, kTrScanPages, (unsigned long long)((n - warp + kScanWarps - 1) / kScanWarps));
+      trace_add(a.err, kTrScanPages, (unsigned long long)((n - grp + ngrp - 1) / ngrp));
     }
     if (c == 0 && (!GRP2 || g < 4)) {
       red[warp][g] = make_float2(zm0, zl0);
@@ -586,25 +608,32 @@ __global__ void __launch_bounds__(kScanThreads, 2) scan_kernel(const ScanArgs a)
   pdl_launch_dependents();
   __syncthreads();
   if (threadIdx.x == 0) trace_max(a.err, kTrScanMaxDur, trace_ns() - t_enter);
-  if (threadIdx.x < G) {
+  // per head of the block: the (max, sum) over its warps' pages
+  for (int t = threadIdx.x; t < HG * G; t += kScanThreads) {
+    const int hw = t / G, gg = t % G;
     float m = -INFINITY, l = 0.f;
-#pragma unroll
-    for (int w = 0; w < kScanWarps; ++w) lse2_merge(m, l, red[w][threadIdx.x].x, red[w][threadIdx.x].y);
-    a.part[((size_t)bh * a.n_chunks + chunk) * G + threadIdx.x] = make_float2(m, l);
+    for (int w = hw; w < kScanWarps; w += HG) lse2_merge(m, l, red[w][gg].x, red[w][gg].y);
+    a.part[((size_t)(b * a.num_kv_heads + h0 + hw) * a.n_chunks + chunk) * G + gg] = make_float2(m, l);
   }
   trace_mark(a.err, kTrScanExit, false);
 }
 
 template <bool G16, bool R16, bool GRP2, bool Q4, int P>
-cudaError_t launch_one(const ScanArgs& a, cudaStream_t s, bool pdl) {
-  const int smem = scan_smem_bytes<R16, Q4>();
-  cudaError_t e =
-      cudaFuncSetAttribute(scan_kernel<G16, R16, GRP2, Q4, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+cudaError_t launch_one(const ScanArgs& a0, cudaStream_t s, bool pdl) {
+  ScanArgs a = a0;
+  const SlotLayout L = slot_layout(a.rank, P, a.heads_per_block, Q4);
+  a.slots = L.slots;
+  a.slot_bytes = L.slot_bytes;
+  a.basis_bytes = L.basis_bytes;
+  a.coef_bytes = L.coef_bytes;
+  if (L.slots < kScanWarps / a.heads_per_block) return cudaErrorInvalidValue;  // the plan keeps slots large enough
+  cudaError_t e = cudaFuncSetAttribute(scan_kernel<G16, R16, GRP2, Q4, P>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.n_chunks, a.batch * a.num_kv_heads, 1);
+  cfg.gridDim = dim3(a.n_chunks, a.batch * (a.num_kv_heads / a.heads_per_block), 1);
   cfg.blockDim = dim3(kScanThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = L.smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
