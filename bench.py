@@ -51,15 +51,12 @@ P, D = 64, 128
 # the scan kernel at each workload; valid only while scan.cu is unchanged
 # since those captures.
 SCAN_TRAFFIC_PER_PAGE_HEAD = {
-    ("llama128k", 64): (50365952 + 2816) / 16384,
-    ("ctx1m", 64): (100761088 + 3253760) / 32768,
-    ("llama128k", 16): (151064832 + 3976448) / 65536,
+    ("llama128k", 64): (50370304 + 1536) / 16384,
+    ("ctx1m", 64): (100765952 + 2990080) / 32768,
 }
-# the same for the quantised summary format
-SCAN_Q4_TRAFFIC_PER_PAGE_HEAD = {
-    ("llama128k", 64): (20229632 + 0) / 16384,
-}
-SCAN_TRAFFIC_SOURCE_SHA = "8ef72a34c0a70c64"
+# the same for the quantised summary format (none captured for this scan.cu)
+SCAN_Q4_TRAFFIC_PER_PAGE_HEAD = {}
+SCAN_TRAFFIC_SOURCE_SHA = "c1a306bcd3246618"
 
 
 # ---------------------------------------------------------------------------
