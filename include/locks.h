@@ -288,11 +288,15 @@ LOCKS_API locks_status_t locks_exact_page_lse(const locks_cache_t* cache, const 
  *
  * Same arguments and results as locks_decode_step, minus the workspace: the
  * step runs in a fixed array of LOCKS_STATIC_WS_BYTES (8 MiB) that the
- * library holds on every GPU it is loaded on, until the process exits.
- * Nothing is allocated or freed: no cudaMalloc, cudaFree or allocating
- * library routine is called.
- *   - The first call on a device (with that device current) looks up the
- *     array's device address; make it before any stream capture begins.
+ * library holds in every CUDA context it is loaded in, until the context
+ * ends.  Nothing is allocated or freed: no cudaMalloc, cudaFree or
+ * allocating library routine is called.
+ *   - Each call made outside stream capture looks up the array's device
+ *     address in the current context (with cudaGetSymbolAddress); a call
+ *     being captured reuses the address of the last uncaptured call on that
+ *     device, and returns LOCKS_ERR_CUDA if there was none.  So make one
+ *     uncaptured call on a device before capturing calls there, and again
+ *     after cudaDeviceReset (which ends the context and its array).
  *   - Each call first zeroes the part of the array these shapes use (one
  *     cudaMemsetAsync on `stream`), so it does not depend on what an earlier
  *     call left there.

@@ -56,6 +56,11 @@ class LocksRuntime:
         off = (-self.ws.data_ptr()) % 256
         self.ws = self.ws[off:off + self.ws_bytes]
         L.locks_workspace_init(self.ws, self.ws_bytes)
+        # the builder's own error word, so that builds may run on another
+        # stream beside calls that use the main workspace
+        self.build_ws = torch.zeros(512, dtype=torch.uint8, device=self.device)
+        off = (-self.build_ws.data_ptr()) % 256
+        self.build_ws = self.build_ws[off:off + 256]
         B = self.batch
         self.sel_pages = torch.zeros((B, hkv, max(self.k_max, 1)), dtype=torch.int32, device=self.device)
         self.sel_count = torch.zeros((B, hkv), dtype=torch.int32, device=self.device)
@@ -71,7 +76,7 @@ class LocksRuntime:
 
     def build_summaries(self, page_ids: torch.Tensor, stream=None):
         ids = page_ids.to(device=self.device, dtype=torch.int32).contiguous()
-        L.locks_build_summaries(self.cache, self.summary, ids, ids.numel(), self.ws, self.ws_bytes, stream)
+        L.locks_build_summaries(self.cache, self.summary, ids, ids.numel(), self.build_ws, 256, stream)
 
     def select(self, q: torch.Tensor, page_lse: torch.Tensor | None = None, stream=None):
         L.locks_select(self.cache, self.summary, self.params, q, self.sel_pages, self.sel_count, page_lse,
@@ -112,4 +117,6 @@ class LocksRuntime:
         return pl
 
     def device_error(self, stream=None) -> int:
-        return L.locks_get_device_error(self.ws, stream)
+        """LOCKS_DEVERR_* bits set since the last read, by the calls on the
+        main workspace and by the builder (both words are cleared)."""
+        return L.locks_get_device_error(self.ws, stream) | L.locks_get_device_error(self.build_ws, stream)

@@ -102,3 +102,41 @@ def test_static_step_rejects_shapes_beyond_its_workspace():
     with pytest.raises(L.LocksError) as e:
         L.locks_decode_step_static(cache, summ, params, q, out, None)
     assert e.value.status == L.LOCKS_ERR_WORKSPACE
+
+
+def test_static_step_allocates_nothing_and_replays_in_a_graph():
+    """Device free memory (cudaMemGetInfo) is unchanged over several static
+    calls after the first, and a call captured in a CUDA graph (after an
+    uncaptured one on the device) gives the uncaptured call's results."""
+    from sparse_kv_page_rank_gb300 import locks as L
+
+    case = make_case(2, 8, 2, [64 * 40 + 3, 64 * 33], true_rank=(4, 10), n_carriers=2, seed=33)
+    rt, q = make_runtime(case, 8, 512)
+    pages = np.concatenate([case.block_table[b, :case.n_full_pages(b)] for b in range(case.batch)])
+    rt.build_summaries(torch.from_numpy(pages.astype(np.int32)).cuda())
+    outs = [(torch.empty_like(rt.out), torch.empty_like(rt.lse), torch.empty_like(rt.sel_pages),
+             torch.empty_like(rt.sel_count), torch.empty((1,), dtype=torch.int32, device="cuda")) for _ in range(2)]
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+
+    def call(o):
+        L.locks_decode_step_static(rt.cache, rt.summary, rt.params, q, o[0], o[1], o[2], o[3], o[4], stream=stream)
+
+    call(outs[0])
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for _ in range(6):
+        call(outs[0])
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert int(outs[0][4].item()) == 0
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            call(outs[1])
+        g.replay()
+    torch.cuda.synchronize()
+    assert int(outs[1][4].item()) == 0
+    for a, b in zip(outs[0][:4], outs[1][:4]):
+        assert torch.equal(a, b)
