@@ -318,12 +318,12 @@ def _config_dict(name, case, cfg, extra=None):
 # GPU arm
 # ---------------------------------------------------------------------------
 
-def _gpu_workload(args, name, K, W, world, dev, *, page_size=P, rank_override=None, full=True):
+def _gpu_workload(args, name, K, W, world, dev, *, page_size=P, rank_override=None, full=True, q4=None):
     """Draw the named workload, build its summaries with the library's builder
     and time (each as one CUDA graph of K calls on R rotating cache copies):
     the decode step, the dense decode and the summary scan alone.  With
-    ``full`` also the end-to-end forms, the quantised format and the clocks.
-    Returns a dict of measurements."""
+    ``full`` also the end-to-end forms; with ``q4`` (default: ``full``) the
+    quantised format.  Returns a dict of measurements."""
     import torch
 
     from sparse_kv_page_rank_gb300.runtime import LocksRuntime
@@ -529,7 +529,7 @@ def _gpu_workload(args, name, K, W, world, dev, *, page_size=P, rank_override=No
     # The quantised, centred summary format (int4 basis, int8 coefficients and
     # centroid) on the same caches: its builder, step and scan.
     res["q4"] = None
-    if full and r <= 8 and not args.no_q4:
+    if (full if q4 is None else q4) and r <= 8 and not args.no_q4:
         from sparse_kv_page_rank_gb300.locks import q4_page_head_bytes
         qrts = [LocksRuntime(rt_.k_pool, rt_.v_pool, bt, sl, ns, Hq, r, budget, quantized=True) for rt_ in rts]
         torch.cuda.synchronize()
@@ -628,7 +628,7 @@ def run_gpu(args):
     # the 1M-context workload beside the 128K headline (step, dense, scan)
     ctx1m = None
     if args.config == "llama128k" and args.page_size == P and not args.rank and not args.no_ctx1m:
-        r1 = _gpu_workload(args, "ctx1m", K, W, world, dev, full=False)
+        r1 = _gpu_workload(args, "ctx1m", K, W, world, dev, full=False, q4=True)
         e1 = r1["step_bytes"]["total"] / (r1["step_ms"] * 1e-3) / 1e9
         ctx1m = {"value": r1["step_ms"] * 1e3, "unit": "us", "config": r1["config"],
                  "step_us_over_replays": r1["step_pct"], "dense_us": r1["dense_ms"] * 1e3,
@@ -637,7 +637,7 @@ def run_gpu(args):
                  "kv_bytes_ratio": r1["dense_bytes"] / r1["step_bytes"]["total"],
                  "mass_recall": r1["mass_recall"], "exact_lse_selection_recall": r1["exact_lse_selection_recall"],
                  "carrier_retention": r1["carrier_retention"], "roofline": _roofline(r1, peak, peak_kind),
-                 "gpu_launches": r1["launches"] * K, "clocks": r1["clocks"],
+                 "gpu_launches": r1["launches"] * K, "clocks": r1["clocks"], "q4": r1["q4"],
                  "timing": {"l2": f"rotating {r1['R']} independent copies of cache + summaries "
                                   f"({r1['R'] * r1['per_copy'] / 1e9:.2f} GB > 129 MB L2)"}}
 

@@ -132,16 +132,21 @@ typedef struct locks_cache {
  *            rank 2..8.  Then basis_t points to one block of
  *            LOCKS_Q4_BLOCK_BYTES(rank, page_size) bytes per page-head,
  *            [pages_total][num_kv_heads][bytes], and coeffs is unused:
- *              byte 0       basis: row j (j < rank) at 64 j; each 32-bit
- *                           little-endian word w holds elements 8m .. 8m+7 of
- *                           the row (m = word index in the row), element 8m+i
- *                           in bits 4(i/2) + 16(i%2) .. +3, as the code + 8
- *                           (codes in [-7, 7])
+ *              byte 0       basis: row j (j < rank) at 64 j, 16 little-endian
+ *                           32-bit words; word m (m = 0..15) holds elements
+ *                           8m .. 8m+7 of the row, element 8m+i in bits
+ *                           4(i/2) + 16(i%2) .. +3, as the code + 8 (codes in
+ *                           [-7, 7]), and sits at word position 4(m%4) + m/4
+ *                           of the row
  *              byte 64r     centroid mu: 128 bytes, code + 128 (codes in
  *                           [-127, 127])
- *              byte 64r+128 coefficients: [page_size][rank] bytes, code + 128
- *              byte 64r+128+P r  float32 scales: basis s_v[rank], coefficients
- *                           s_c[rank], centroid s_mu
+ *              byte 64r+128 coefficients: P r bytes, code + 128; the code of
+ *                           token i, column j at byte
+ *                           (((i%8) (r/2) + j/2) (P/8) + i/8) 2 + j%2
+ *              byte 64r+128+P r  float32 scales: for each column pair
+ *                           t = 0 .. r/2-1 the four values s_v[2t],
+ *                           s_v[2t+1], s_c[2t], s_c[2t+1]; then s_mu
+ *            (the orders put the pieces one GPU lane needs side by side).
  *            The summary stands for V_j = s_v[j] * code, c_i[j] = s_c[j] *
  *            code, mu = s_mu * code, and the page's keys are approximated
  *            by mu + sum_j c_i[j] V_j (centred). */

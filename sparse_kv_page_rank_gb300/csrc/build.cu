@@ -428,7 +428,8 @@ __global__ void __launch_bounds__(kBT) build_kernel(const BuildArgs a) {
     };
     uint8_t* blk = static_cast<uint8_t*>(a.basis_t) + ph * (size_t)LOCKS_Q4_BLOCK_BYTES(r, P);
     // basis: word m of row j holds elements 8m .. 8m+7, element 8m+i at
-    // bits 4(i/2) + 16(i%2), as code + 8
+    // bits 4(i/2) + 16(i%2), as code + 8; it is stored at word 4(m%4) + m/4
+    // of the row, so the four words one scan lane reads are adjacent
     uint32_t* bw = reinterpret_cast<uint32_t*>(blk);
     for (int e = tid; e < r * (kHeadDim / 8); e += kBT) {
       const int j = e / (kHeadDim / 8), m = e % (kHeadDim / 8);
@@ -436,13 +437,22 @@ __global__ void __launch_bounds__(kBT) build_kernel(const BuildArgs a) {
 #pragma unroll
       for (int i = 0; i < 8; ++i)
         w |= (uint32_t)(code(s.V[j * kVS + 8 * m + i], s.sv[j], 7.f) + 8) << (4 * (i / 2) + 16 * (i % 2));
-      bw[e] = w;
+      bw[j * (kHeadDim / 8) + 4 * (m % 4) + m / 4] = w;
     }
     for (int k = tid; k < kHeadDim; k += kBT) blk[64 * r + k] = (uint8_t)(code(s.mu[k], s.smu, 127.f) + 128);
-    for (int e = tid; e < P * r; e += kBT)
-      blk[64 * r + kHeadDim + e] = (uint8_t)(code(s.Y[(e / r) * kXS + e % r], s.sc[e % r], 127.f) + 128);
+    // coefficients: token i, column j at (((i%8) r/2 + j/2) P/8 + i/8) 2 + j%2
+    // (the codes of tokens i%8 + 8t, columns 2c and 2c+1, side by side)
+    for (int e = tid; e < P * r; e += kBT) {
+      const int i = e / r, j = e % r;
+      const int at = (((i % 8) * (r / 2) + j / 2) * (P / 8) + i / 8) * 2 + j % 2;
+      blk[64 * r + kHeadDim + at] = (uint8_t)(code(s.Y[i * kXS + j], s.sc[j], 127.f) + 128);
+    }
+    // scales: per column pair t, s_v[2t], s_v[2t+1], s_c[2t], s_c[2t+1]; then s_mu
     float* sco = reinterpret_cast<float*>(blk + 64 * r + kHeadDim + P * r);
-    for (int e = tid; e < 2 * r + 1; e += kBT) sco[e] = e < r ? s.sv[e] : (e < 2 * r ? s.sc[e - r] : s.smu);
+    for (int e = tid; e < 2 * r + 1; e += kBT) {
+      const int t = e / 4, u = e % 4;
+      sco[e] = e == 2 * r ? s.smu : (u < 2 ? s.sv[2 * t + u] : s.sc[2 * t + u - 2]);
+    }
   } else if (a.format == LOCKS_DTYPE_F32) {
     float* bo = reinterpret_cast<float*>(a.basis_t) + ph * (size_t)r * kHeadDim;
     float* co = reinterpret_cast<float*>(a.coeffs) + ph * (size_t)P * r;

@@ -45,6 +45,23 @@ __device__ __forceinline__ void mma_1688(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(b0));
 }
 
+// The same two shapes with fp16 operands.
+__device__ __forceinline__ void mma_16816_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma_1688_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(b0));
+}
+
 __device__ __forceinline__ void ldmatrix_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3,
                                             uint32_t addr) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
@@ -225,6 +242,26 @@ __device__ __forceinline__ uint32_t u8pair_bf16(uint32_t w, int k) {
   const float lo = __uint_as_float(__byte_perm(w, 0x4b000000u, 0x7650u + k)) - 8388736.f;
   const float hi = __uint_as_float(__byte_perm(w, 0x4b000000u, 0x7651u + k)) - 8388736.f;
   return __byte_perm(__float_as_uint(lo), __float_as_uint(hi), 0x7632u);
+}
+
+// Four 8-bit codes stored as code + 128 in the bytes of w -> two fp16 pairs
+// (bytes 0, 1 -> lo; bytes 2, 3 -> hi): a byte under the fp16 exponent of
+// 1024 is the exact number 1024 + byte, from which 1152 = 1024 + 128 is
+// subtracted.
+__device__ __forceinline__ void u8quad_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  lo = __byte_perm(w, 0x64646464u, 0x4140u);
+  hi = __byte_perm(w, 0x64646464u, 0x4342u);
+  asm("sub.rn.f16x2 %0, %0, %2;\n sub.rn.f16x2 %1, %1, %2;\n" : "+r"(lo), "+r"(hi) : "r"(0x64806480u));
+}
+// (x0, x1) -> hi + lo as fp16 pairs (x0 in the low halves): hi rounds x to
+// fp16, saturating at +-65504, and lo rounds the remainder (about 22 bits
+// of x together).
+__device__ __forceinline__ void split2_f16(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;\n" : "=r"(hi) : "f"(x1), "f"(x0));
+  float h0, h1;
+  asm("{\n .reg .f16 a, b;\n mov.b32 {a, b}, %2;\n cvt.f32.f16 %0, a;\n cvt.f32.f16 %1, b;\n}\n"
+      : "=f"(h0), "=f"(h1) : "r"(hi));
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;\n" : "=r"(lo) : "f"(x1 - h1), "f"(x0 - h0));
 }
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {

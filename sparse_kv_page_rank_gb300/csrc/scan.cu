@@ -260,57 +260,73 @@ __device__ __forceinline__ void compute_page(uint32_t bas, uint32_t coef, const 
 }
 
 // The same page-head estimate from the quantised, centred format (int4 basis
-// codes, int8 centroid and coefficient codes, float32 scales; rank <= 8):
-// the codes are exact in bf16, so the contractions run on them directly and
-// the scales enter in fp32 -- each basis vector's and coefficient column's
-// scale on its column of W.  Returns the LSE of the centred logits; q . mu
-// shifts every logit of the head alike and is added later (mu_batch).
+// codes, int8 centroid and coefficient codes, float32 scales; rank <= 8).
+// The block's layout puts what one lane needs side by side: its four basis
+// words, its coefficient codes and its two columns' scales are one 16-byte
+// load each.  (1) runs on the basis codes in bf16 (exact: small integers),
+// each basis vector's and coefficient column's scale is applied in fp32 on
+// its column of W, and (2) runs in fp16: a byte code becomes an exact fp16 in
+// two instructions per pair, and W is split into two fp16 terms (hi + lo,
+// about 22 bits; hi saturates at +-65504, a logit contribution per code unit
+// far beyond any softmax-relevant range).  Returns the LSE of the centred
+// logits; q . mu shifts every logit of the head alike and is added later
+// (mu_batch).
 template <bool G16, bool GRP2, int P>
 __device__ __forceinline__ void compute_page_q4(uint32_t slot, const uint4 (&qa)[4], const uint4 (&qb)[4], int r,
                                                 float scale_log2, int lane, float& e0, float& e1) {
   constexpr int NT = P / 8;
   const int g = lane >> 2, c = lane & 3;
+  const int rh = r >> 1;  // column pairs
   const uint32_t coef_off = 64 * r + kHeadDim, sc_off = 64 * r + kHeadDim + P * r;
-  // (1) W^T = Q V on the basis codes
+  // (1) W^T = Q V on the basis codes: row g's words for elements 32s + 8c ..
+  // +7, s = 0..3 (a row past the rank reads as all-zero codes)
+  const uint4 nib = (g < r) ? lds128(slot + 64 * g + 16 * c) : make_uint4(0x88888888u, 0x88888888u, 0x88888888u,
+                                                                            0x88888888u);
+  const uint32_t nw[4] = {nib.x, nib.y, nib.z, nib.w};
   float w0[4] = {0.f, 0.f, 0.f, 0.f}, x0[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
-    // elements 32s + 8c .. +7 of basis row g: one word of biased nibbles
-    // (a row past the rank reads as all-zero codes)
-    const uint32_t nib = (g < r) ? lds32(slot + 64 * g + 16 * s + 4 * c) : 0x88888888u;
-    mma_16816(w0, qa[s].x, qb[s].x, qa[s].y, qb[s].y, u4pair_bf16(nib, 0), u4pair_bf16(nib, 4));
-    mma_16816(x0, qa[s].z, qb[s].z, qa[s].w, qb[s].w, u4pair_bf16(nib, 8), u4pair_bf16(nib, 12));
+    mma_16816(w0, qa[s].x, qb[s].x, qa[s].y, qb[s].y, u4pair_bf16(nw[s], 0), u4pair_bf16(nw[s], 4));
+    mma_16816(x0, qa[s].z, qb[s].z, qa[s].w, qb[s].w, u4pair_bf16(nw[s], 8), u4pair_bf16(nw[s], 12));
   }
-  // column j of W gets s_v[j] * s_c[j] (and the base-2 logit scale)
-  const int j0 = 2 * c, j1 = 2 * c + 1;
-  const float f0 = j0 < r ? __uint_as_float(lds32(slot + sc_off + 4 * j0)) *
-                                __uint_as_float(lds32(slot + sc_off + 4 * (r + j0))) * scale_log2
-                          : 0.f;
-  const float f1 = j1 < r ? __uint_as_float(lds32(slot + sc_off + 4 * j1)) *
-                                __uint_as_float(lds32(slot + sc_off + 4 * (r + j1))) * scale_log2
-                          : 0.f;
+  // column 2c of W gets s_v[2c] s_c[2c], column 2c+1 likewise (and the
+  // base-2 logit scale); this lane's coefficient codes: tokens g + 8t,
+  // columns 2c, 2c+1, two bytes per n-tile t
+  const bool has = c < rh;
+  const uint4 sc4 = has ? lds128(slot + sc_off + 16 * c) : make_uint4(0u, 0u, 0u, 0u);
+  const float f0 = __uint_as_float(sc4.x) * __uint_as_float(sc4.z) * scale_log2;
+  const float f1 = __uint_as_float(sc4.y) * __uint_as_float(sc4.w) * scale_log2;
+  uint32_t cw[(NT + 1) / 2];
+  if constexpr (NT == 8) {
+    const uint4 t = has ? lds128(slot + coef_off + 16 * (g * rh + c)) : make_uint4(0x80808080u, 0x80808080u,
+                                                                                     0x80808080u, 0x80808080u);
+    cw[0] = t.x;
+    cw[1] = t.y;
+    cw[2] = t.z;
+    cw[3] = t.w;
+  } else {
+    static_assert(NT == 2, "64- or 16-token pages");
+    cw[0] = has ? lds32(slot + coef_off + 4 * (g * rh + c)) : 0x80808080u;
+  }
+  uint32_t cb[NT];  // fp16 pair for n-tile t: (token g + 8t; columns 2c, 2c+1)
+#pragma unroll
+  for (int u = 0; u < NT / 2; ++u) u8quad_f16(cw[u], cb[2 * u], cb[2 * u + 1]);
   const float wa = (w0[0] + x0[0]) * f0, wb = (w0[1] + x0[1]) * f1;
   const float wc = (w0[2] + x0[2]) * f0, wd = (w0[3] + x0[3]) * f1;
-  auto coef = [&](int jt) -> uint32_t {
-    return (2 * c < r) ? u8pair_bf16(lds16(slot + coef_off + (8 * jt + g) * r + 2 * c), 0) : 0u;
-  };
 
   if (GRP2) {
     uint32_t hh, mm;
-    split2(wa, wb, hh, mm);
+    split2_f16(wa, wb, hh, mm);
     const bool lo_half = lane < 16;
     const uint32_t ha0 = lo_half ? hh : 0u, ha2 = lo_half ? 0u : hh;
     const uint32_t ma0 = lo_half ? mm : 0u, ma2 = lo_half ? 0u : mm;
-    uint32_t cbv[NT];
-#pragma unroll
-    for (int jt = 0; jt < NT; ++jt) cbv[jt] = coef(jt);
     float d[NT / 2][4];
     float v[NT];
 #pragma unroll
     for (int jt = 0; jt < NT / 2; ++jt) {
       d[jt][0] = d[jt][1] = d[jt][2] = d[jt][3] = 0.f;
-      mma_16816(d[jt], ma0, 0u, ma2, 0u, cbv[2 * jt], cbv[2 * jt + 1]);
-      mma_16816(d[jt], ha0, 0u, ha2, 0u, cbv[2 * jt], cbv[2 * jt + 1]);
+      mma_16816_f16(d[jt], ma0, 0u, ma2, 0u, cb[2 * jt], cb[2 * jt + 1]);
+      mma_16816_f16(d[jt], ha0, 0u, ha2, 0u, cb[2 * jt], cb[2 * jt + 1]);
       v[2 * jt] = d[jt][0];
       v[2 * jt + 1] = d[jt][1];
     }
@@ -320,17 +336,14 @@ __device__ __forceinline__ void compute_page_q4(uint32_t slot, const uint4 (&qa)
   }
 
   uint32_t h0, m0, h1, m1;
-  split2(wa, wb, h0, m0);
-  split2(wc, wd, h1, m1);
-  uint32_t cb[NT];
-#pragma unroll
-  for (int jt = 0; jt < NT; ++jt) cb[jt] = coef(jt);
+  split2_f16(wa, wb, h0, m0);
+  split2_f16(wc, wd, h1, m1);
   float d[NT][4];
 #pragma unroll
   for (int jt = 0; jt < NT; ++jt) {
     d[jt][0] = d[jt][1] = d[jt][2] = d[jt][3] = 0.f;
-    mma_1688(d[jt], m0, m1, cb[jt]);
-    mma_1688(d[jt], h0, h1, cb[jt]);
+    mma_1688_f16(d[jt], m0, m1, cb[jt]);
+    mma_1688_f16(d[jt], h0, h1, cb[jt]);
   }
   float v[2 * NT];
 #pragma unroll

@@ -36,20 +36,46 @@ def q4_block_bytes(r: int, P: int = 64) -> int:
     return (64 * r + 128 + P * r + 4 * (2 * r + 1) + 15) // 16 * 16
 
 
+def _q4_word_position(m):
+    """Word m of a basis row sits at word 4(m%4) + m/4 of the row."""
+    return 4 * (m % 4) + m // 4
+
+
+def _q4_coef_position(i, j, r, P):
+    """Byte of the code of token i, column j in the coefficient block."""
+    return (((i % 8) * (r // 2) + j // 2) * (P // 8) + i // 8) * 2 + j % 2
+
+
+def _q4_scale_order(r):
+    """Float index -> (which, column): per column pair t, s_v[2t], s_v[2t+1],
+    s_c[2t], s_c[2t+1]; then s_mu."""
+    order = []
+    for t in range(r // 2):
+        order += [("sv", 2 * t), ("sv", 2 * t + 1), ("sc", 2 * t), ("sc", 2 * t + 1)]
+    return order + [("smu", 0)]
+
+
 def pack_q4(qs: dict, r: int) -> np.ndarray:
     """One oracle-quantised page-head summary in the LOCKS_DTYPE_Q4 byte layout
-    (the page size is the coefficient block's row count)."""
+    of include/locks.h (the page size is the coefficient block's row count)."""
     P = np.asarray(qs["cq"]).shape[0]
     buf = np.zeros(q4_block_bytes(r, P), dtype=np.uint8)
     u = (np.asarray(qs["vq"]) + 8).astype(np.uint32).reshape(r, 16, 8)  # [row][word][element], code + 8
     words = np.zeros((r, 16), dtype=np.uint32)
     for i in range(8):
         words |= u[:, :, i] << np.uint32(4 * (i // 2) + 16 * (i % 2))
-    buf[:64 * r] = words.astype("<u4").view(np.uint8).reshape(-1)
+    placed = np.zeros_like(words)
+    for m in range(16):
+        placed[:, _q4_word_position(m)] = words[:, m]
+    buf[:64 * r] = placed.astype("<u4").view(np.uint8).reshape(-1)
     buf[64 * r:64 * r + 128] = (np.asarray(qs["muq"]) + 128).astype(np.uint8)
     c0 = 64 * r + 128
-    buf[c0:c0 + P * r] = (np.asarray(qs["cq"]) + 128).astype(np.uint8).reshape(-1)
-    scales = np.concatenate([qs["sv"], qs["sc"], [qs["smu"]]]).astype(np.float32)
+    cq = np.asarray(qs["cq"])
+    for i in range(P):
+        for j in range(r):
+            buf[c0 + _q4_coef_position(i, j, r, P)] = cq[i, j] + 128
+    vals = {"sv": np.asarray(qs["sv"]), "sc": np.asarray(qs["sc"]), "smu": np.asarray([qs["smu"]])}
+    scales = np.array([vals[w][c] for w, c in _q4_scale_order(r)], dtype=np.float32)
     buf[c0 + P * r:c0 + P * r + 4 * (2 * r + 1)] = scales.view(np.uint8)
     return buf
 
@@ -57,16 +83,26 @@ def pack_q4(qs: dict, r: int) -> np.ndarray:
 def unpack_q4(buf: np.ndarray, r: int, P: int = 64, d: int = 128) -> dict:
     """Inverse of pack_q4 (reads the ABI layout back into codes and scales)."""
     buf = np.asarray(buf, dtype=np.uint8)
-    words = buf[:64 * r].copy().view("<u4").reshape(r, d // 8).astype(np.int64)
+    placed = buf[:64 * r].copy().view("<u4").reshape(r, d // 8).astype(np.int64)
+    words = np.stack([placed[:, _q4_word_position(m)] for m in range(d // 8)], axis=1)
     vq = np.empty((r, d // 8, 8), dtype=np.int64)
     for i in range(8):
         vq[:, :, i] = ((words >> (4 * (i // 2) + 16 * (i % 2))) & 15) - 8
     vq = vq.reshape(r, d)
     muq = buf[64 * r:64 * r + 128].astype(np.int64) - 128
     c0 = 64 * r + 128
-    cq = (buf[c0:c0 + P * r].astype(np.int64) - 128).reshape(P, r)
-    sc = buf[c0 + P * r:c0 + P * r + 4 * (2 * r + 1)].view(np.float32).astype(np.float64)
-    return dict(vq=vq, sv=sc[:r], cq=cq, sc=sc[r:2 * r], muq=muq, smu=float(sc[2 * r]))
+    cq = np.empty((P, r), dtype=np.int64)
+    for i in range(P):
+        for j in range(r):
+            cq[i, j] = int(buf[c0 + _q4_coef_position(i, j, r, P)]) - 128
+    flat = buf[c0 + P * r:c0 + P * r + 4 * (2 * r + 1)].view(np.float32).astype(np.float64)
+    out = {"sv": np.zeros(r), "sc": np.zeros(r), "smu": 0.0}
+    for f, (w, c) in zip(flat, _q4_scale_order(r)):
+        if w == "smu":
+            out["smu"] = float(f)
+        else:
+            out[w][c] = f
+    return dict(vq=vq, sv=out["sv"], cq=cq, sc=out["sc"], muq=muq, smu=out["smu"])
 
 
 def oracle_summaries_q4(case, r: int, heads=None, pages=None):
