@@ -439,18 +439,18 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(const ScanArgs a)
 #pragma unroll
     for (int u = 0; u < kPre; ++u) pre[u] = (lane < S && lane + u * S < n) ? bt[j0 + lane + u * S] : -1;
     int p = lane < S ? lane : n;  // next page of this lane
+    int u = 0;                    // its round: p = lane + u S
     for (uint32_t spin = 0; __any_sync(0xffffffffu, p < n); ++spin) {
       if (spin == kMbarSpinLimit * 4u) {
         if (lane == 0) set_error(a.err, kDevErrTimeout);
         break;
       }
-      const bool ready = p < n && (p < S || mbar_test(&empty_bar[lane], (uint32_t)(((p / S) - 1) & 1)));
+      const bool ready = p < n && (u == 0 || mbar_test(&empty_bar[lane], (uint32_t)((u - 1) & 1)));
       if (!__any_sync(0xffffffffu, ready)) {
         __nanosleep(64);
         continue;
       }
       if (ready) {
-        const int u = p / S;
         int phys = -1;
 #pragma unroll
         for (int v = 0; v < kPre; ++v)
@@ -470,6 +470,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(const ScanArgs a)
           mbar_arrive(&full_bar[lane]);
         }
         p += S;
+        ++u;
       }
     }
   } else {
@@ -542,10 +543,18 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(const ScanArgs a)
       npend = 0;
       vmask = 0;
     };
-    for (int p = grp; p < n; p += ngrp) {
-      const int s = p % S;
+    // slot s = p mod S and phase parity (p / S) & 1 of page p, advanced
+    // without dividing: S is a multiple of ngrp, so s wraps exactly when p
+    // crosses a multiple of S
+    int s = grp;
+    uint32_t phase = 0;
+    for (int p = grp; p < n; p += ngrp, s += ngrp) {
+      if (s >= S) {
+        s -= S;
+        phase ^= 1u;
+      }
       const unsigned long long t0 = trace_clock();
-      const bool ok = mbar_wait(&full_bar[s], (uint32_t)((p / S) & 1));
+      const bool ok = mbar_wait(&full_bar[s], phase);
       const unsigned long long t1 = trace_clock();
       if (__any_sync(0xffffffffu, !ok)) {
         if (lane == 0) set_error(a.err, kDevErrTimeout);
