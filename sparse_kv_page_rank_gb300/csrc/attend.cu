@@ -535,14 +535,23 @@ __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_con
     if (SPL) trace_mark(a.err, kTrAttWait, true);
     clamp_lengths();
     const int n_pages = (L + P - 1) / P;
+    int cnt_written = 0;
     if (MODE == kAttendSparse) {
       const int cap = min(L / P, a.max_pages);
       ns = ns_raw < 0 ? 0 : (ns_raw > cap ? cap : ns_raw);
-      cnt = a.sel_count[bh];
       const int kcap = min(a.k_max, ns);
-      if (cnt < 0 || cnt > kcap) {
-        if (tid == 0) set_error(a.err, LOCKS_DEVERR_SEL_PAGE);
-        cnt = cnt < 0 ? 0 : kcap;
+      if (a.inputs_early) {
+        // inside the decode step the top-k writes exactly min(k_max, ns)
+        // pages, so the page list is read without first waiting for the
+        // count; the count it wrote is loaded alongside and checked
+        cnt = kcap;
+        cnt_written = a.sel_count[bh];
+      } else {
+        cnt = a.sel_count[bh];
+        if (cnt < 0 || cnt > kcap) {
+          if (tid == 0) set_error(a.err, LOCKS_DEVERR_SEL_PAGE);
+          cnt = cnt < 0 ? 0 : kcap;
+        }
       }
       n_items = cnt + (n_pages - ns);
     } else {
@@ -550,6 +559,7 @@ __global__ void __launch_bounds__(kAttendThreads) attend_kernel(const __grid_con
     }
     set_range();
     resolve(0);
+    if (MODE == kAttendSparse && a.inputs_early && tid == 0 && cnt_written != cnt) set_error(a.err, LOCKS_DEVERR_SEL_PAGE);
     __syncthreads();
   }
   if (SPL) trace_mark(a.err, kTrAttResolved, false);
