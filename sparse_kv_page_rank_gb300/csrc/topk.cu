@@ -429,11 +429,14 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkArgs a)
   // ---- one round trip: lengths, scan partials (warp h: head h), s_hat rows
   const int L = a.seq_lens[b];
   int ns = a.n_summarized[b];
-  float2 pv[4];
+  // the scan writes one partial per chunk, at most one chunk per SM (152 on
+  // GB300): five per lane load them all in the first round trip
+  constexpr int kPv = 5;
+  float2 pv[kPv];
   const float2* pbase = a.part + (size_t)bh * a.n_scan_chunks * G;
   if (warp < G) {
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < kPv; ++u) {
       const int i = lane + 32 * u;
       pv[u] = i < a.n_scan_chunks ? __ldcg(pbase + (size_t)i * G + warp) : make_float2(-INFINITY, 0.f);
     }
@@ -488,8 +491,8 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkArgs a)
   if (warp < G) {
     float m = -INFINITY, l = 0.f;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) lse2_merge(m, l, pv[u].x, pv[u].y);
-    for (int i = lane + 128; i < a.n_scan_chunks; i += 32) {
+    for (int u = 0; u < kPv; ++u) lse2_merge(m, l, pv[u].x, pv[u].y);
+    for (int i = lane + 32 * kPv; i < a.n_scan_chunks; i += 32) {
       const float2 v = __ldcg(pbase + (size_t)i * G + warp);
       lse2_merge(m, l, v.x, v.y);
     }
