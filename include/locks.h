@@ -167,14 +167,14 @@ typedef struct locks_params {
   int32_t flags;   /* 0, LOCKS_FLAG_UNFUSED or LOCKS_FLAG_FUSED; other bits are reserved and must be 0 */
 } locks_params_t;
 
-/* locks_decode_step runs as two kernels when page_size is 64, k_max <= 32,
- * max_pages <= 128 x (the largest thread-block cluster, 16 CTAs) and there
- * are more (sequence, KV head) problems than SMs: the summary scan, then one
- * attention kernel whose clusters compute the group-shared top-k themselves.
- * Otherwise it runs three kernels (scan, top-k, attention).  Both forms
- * select the same pages.  LOCKS_FLAG_UNFUSED always takes the three-kernel
- * form; LOCKS_FLAG_FUSED takes the two-kernel form whenever the size limits
- * allow, whatever the number of problems.  Setting both is an error. */
+/* locks_decode_step runs as three kernels (summary scan, top-k, attention).
+ * With LOCKS_FLAG_FUSED it runs as two when page_size is 64, k_max <= 32 and
+ * max_pages <= 128 x (the largest thread-block cluster, 16 CTAs): the scan,
+ * then one attention kernel whose clusters compute the group-shared top-k
+ * themselves.  Both forms select the same pages; on GB300 the three-kernel
+ * form is the faster one at every measured shape (1 to 256 problems).
+ * LOCKS_FLAG_UNFUSED asks for the three-kernel form explicitly.  Setting both
+ * is an error. */
 #define LOCKS_FLAG_UNFUSED 0x1
 #define LOCKS_FLAG_FUSED 0x2
 
@@ -250,8 +250,8 @@ LOCKS_API locks_status_t locks_sparse_attend(const locks_cache_t* cache, const l
  * between the launches, programmatic dependent launch between kernels).
  * sel_pages / sel_count may be NULL (then kept in the workspace); when given
  * they receive the page list as locks_select writes it.  This is the whole
- * decode step; capture it in a CUDA graph for replay.  Where the shapes allow
- * (see LOCKS_FLAG_UNFUSED) the top-k runs inside the attention kernel: each
+ * decode step; capture it in a CUDA graph for replay.  With LOCKS_FLAG_FUSED,
+ * where the shapes allow, the top-k runs inside the attention kernel: each
  * sequence's thread-block cluster scores its pages, exchanges its best
  * candidates through distributed shared memory and attends to the pages it
  * selected, and the K/V of the open tail is loaded while the scan is still
@@ -261,9 +261,10 @@ LOCKS_API locks_status_t locks_decode_step(const locks_cache_t* cache, const loc
                                  float* lse, int32_t* sel_pages, int32_t* sel_count,
                                  void* ws, size_t ws_bytes, void* stream);
 
-/* Number of kernels one locks_decode_step launches for these shapes: 2 (the
- * scan, then attention with the top-k inside its clusters) or 3 (scan, top-k,
- * attention); see LOCKS_FLAG_UNFUSED.  Host only; launches nothing. */
+/* Number of kernels one locks_decode_step launches for these shapes and
+ * flags: 2 (the scan, then attention with the top-k inside its clusters) or 3
+ * (scan, top-k, attention); see LOCKS_FLAG_FUSED.  Host only; launches
+ * nothing. */
 LOCKS_API locks_status_t locks_decode_step_launches(const locks_cache_t* cache, const locks_summary_t* summary,
                                                     const locks_params_t* params, int32_t* launches);
 

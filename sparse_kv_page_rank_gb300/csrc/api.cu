@@ -163,14 +163,13 @@ Plan make_plan(const locks_cache_t* c, const locks_params_t* p) {
     pl.lse_splits = (int)std::max<long long>(1, std::min<long long>(ls, max_tiles));
     // fused step (64-token pages, k <= kFusedMaxK): one cluster per problem
     // whose CTAs score at most one page per thread; sized like the sparse
-    // cluster, then raised until the pages fit.  Taken when there are more
-    // problems than SMs: the separate top-k (one 512-thread CTA per SM) would
-    // then need more than one wave, while with few problems its 16 warps per
-    // CTA select faster than the 4-warp attention CTAs do (measured on GB300:
-    // 128K context, 8 problems, 24.6 us with the separate top-k and 27.6 us
-    // fused; 8K context, 256 problems, 62.7 us and 59.7 us).
-    if (P == kPage && pl.k_max <= kFusedMaxK && !(p->flags & LOCKS_FLAG_UNFUSED) &&
-        (BH > sms || (p->flags & LOCKS_FLAG_FUSED))) {
+    // cluster, then raised until the pages fit.  Taken only on request
+    // (LOCKS_FLAG_FUSED): the separate top-k, 512 threads per problem,
+    // selects faster than the 4-warp attention CTAs do, at every measured
+    // problem count (GB300: 8K context with 256 problems, 50.3 us with the
+    // separate top-k and 52.0 us fused; 32K with 64 problems, 34.4 and 37.5;
+    // 128K with 8 problems, 23.7 and 29.4).
+    if (P == kPage && pl.k_max <= kFusedMaxK && (p->flags & LOCKS_FLAG_FUSED)) {
       const int cs_max = attend_max_cluster(kAttendFused, P);
       const long long need = ((long long)c->max_pages + kAttendThreads - 1) / kAttendThreads;
       int csf = 1;

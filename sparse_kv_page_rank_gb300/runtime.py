@@ -20,8 +20,9 @@ class LocksRuntime:
     Summaries are allocated here: bf16 [pages_total][Hkv][rank][128] and
     [..][P][rank], or, with ``quantized``, one packed LOCKS_DTYPE_Q4 block per
     page-head (uint8 [pages_total][Hkv][q4_page_head_bytes(rank, P)]).
-    ``form``: "auto", or "unfused" / "fused" for LOCKS_FLAG_UNFUSED / LOCKS_FLAG_FUSED
-    (the decode step as three kernels, or as two wherever the size limits allow).
+    ``form``: "auto" (the library's choice: three kernels), or "unfused" /
+    "fused" for LOCKS_FLAG_UNFUSED / LOCKS_FLAG_FUSED (the decode step as three
+    kernels, or as two wherever the size limits allow).
     """
 
     def __init__(self, k_pool: torch.Tensor, v_pool: torch.Tensor, block_table: torch.Tensor,

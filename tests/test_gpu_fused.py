@@ -1,11 +1,10 @@
 """The decode step with the top-k inside the attention kernel (GPU).
 
-locks_decode_step runs as two kernels (the scan, then attention whose
-thread-block clusters compute the group-shared top-k themselves) for 64-token
-pages with k_max <= 32, at most 128 pages per CTA of a 16-CTA cluster and more
-(sequence, KV head) problems than SMs, and as three kernels (scan, top-k,
-attention) otherwise or with LOCKS_FLAG_UNFUSED.  The cases here force the
-two-kernel form with LOCKS_FLAG_FUSED.  Both forms are checked against the fp64 oracle with the
+With LOCKS_FLAG_FUSED, locks_decode_step runs as two kernels (the scan, then
+attention whose thread-block clusters compute the group-shared top-k
+themselves) for 64-token pages with k_max <= 32 and at most 128 pages per CTA
+of a 16-CTA cluster; otherwise, and by default, as three kernels (scan, top-k,
+attention).  Both forms are checked against the fp64 oracle with the
 tolerances of test_gpu_parity (page LSE 1e-3 relative, selection bit-exact
 outside a 1e-4 band around the cut, output 1e-2 absolute, lse 1e-3 relative),
 and against each other: the same pages, and outputs within 1e-2.
@@ -185,14 +184,16 @@ def test_fused_step_llama128k_sampled():
         assert np.all(np.abs(fl[b, hs] - rl[0]) <= LSE_RTOL * np.maximum(1.0, np.abs(rl[0])))
 
 
-def test_automatic_form_follows_the_problem_count():
-    """Without a flag, the two-kernel form is taken when there are more
-    (sequence, KV head) problems than SMs, and not otherwise."""
+def test_default_form_is_three_kernels():
+    """Without a flag the step takes the three-kernel form, whatever the
+    number of (sequence, KV head) problems; LOCKS_FLAG_FUSED takes the
+    two-kernel form within its limits."""
     from sparse_kv_page_rank_gb300.runtime import LocksRuntime
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    for batch, expect in ((1, 3), (sms // 8 + 1, 2)):
+    for batch in (1, sms // 8 + 1):
         k = torch.zeros((4 * batch, 8, 64, 128), dtype=torch.bfloat16, device="cuda")
         bt = torch.arange(4 * batch, dtype=torch.int32, device="cuda").view(batch, 4)
         sl = torch.full((batch,), 256, dtype=torch.int32, device="cuda")
-        rt = LocksRuntime(k, k, bt, sl, torch.full((batch,), 4, dtype=torch.int32, device="cuda"), 32, 8, 128)
-        assert rt.decode_step_launches() == expect, (batch, sms)
+        ns = torch.full((batch,), 4, dtype=torch.int32, device="cuda")
+        assert LocksRuntime(k, k, bt, sl, ns, 32, 8, 128).decode_step_launches() == 3, (batch, sms)
+        assert LocksRuntime(k, k, bt, sl, ns, 32, 8, 128, form="fused").decode_step_launches() == 2, (batch, sms)
