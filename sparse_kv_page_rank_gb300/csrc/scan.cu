@@ -438,6 +438,9 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(const ScanArgs a)
     int pre[kPre];
 #pragma unroll
     for (int u = 0; u < kPre; ++u) pre[u] = (lane < S && lane + u * S < n) ? bt[j0 + lane + u * S] : -1;
+    // every summary is read once per step: first to leave L2, so that the
+    // s_hat rows written here stay there for the top-k
+    const uint64_t once = l2_policy_evict_first();
     int p = lane < S ? lane : n;  // next page of this lane
     int u = 0;                    // its round: p = lane + u S
     for (uint32_t spin = 0; __any_sync(0xffffffffu, p < n); ++spin) {
@@ -463,9 +466,11 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(const ScanArgs a)
           const size_t ph = (size_t)phys * a.num_kv_heads + h0;
           const uint32_t slot = ring + lane * slot_bytes;
           mbar_arrive_expect_tx(&full_bar[lane], bb + cb);
-          bulk_load(slot, reinterpret_cast<const uint8_t*>(a.basis_t) + ph * a.basis_bytes, bb, &full_bar[lane]);
+          bulk_load_hint(slot, reinterpret_cast<const uint8_t*>(a.basis_t) + ph * a.basis_bytes, bb, &full_bar[lane],
+                         once);
           if (!Q4)
-            bulk_load(slot + bb, reinterpret_cast<const uint8_t*>(a.coeffs) + ph * a.coef_bytes, cb, &full_bar[lane]);
+            bulk_load_hint(slot + bb, reinterpret_cast<const uint8_t*>(a.coeffs) + ph * a.coef_bytes, cb,
+                           &full_bar[lane], once);
         } else {
           mbar_arrive(&full_bar[lane]);
         }
