@@ -51,15 +51,15 @@ P, D = 64, 128
 # the scan kernel at each workload; valid only while scan.cu is unchanged
 # since those captures.
 SCAN_TRAFFIC_PER_PAGE_HEAD = {
-    ("llama128k", 64): (50368512 + 2816) / 16384,
-    ("ctx1m", 64): (100762624 + 2873088) / 32768,
+    ("llama128k", 64): (50368768 + 4864) / 16384,
+    ("ctx1m", 64): (100764160 + 2743296) / 32768,
 }
 # the same for the quantised summary format
 SCAN_Q4_TRAFFIC_PER_PAGE_HEAD = {
-    ("llama128k", 64): (20231680 + 0) / 16384,
-    ("ctx1m", 64): (40477952 + 1792) / 32768,
+    ("llama128k", 64): (20231936 + 0) / 16384,
+    ("ctx1m", 64): (40477952 + 256) / 32768,
 }
-SCAN_TRAFFIC_SOURCE_SHA = "c2f6553c8aa0ca5e"
+SCAN_TRAFFIC_SOURCE_SHA = "869a9d1c61331791"
 
 
 # ---------------------------------------------------------------------------
