@@ -87,6 +87,7 @@ typedef enum {
 #define LOCKS_DTYPE_BF16 0
 #define LOCKS_DTYPE_F32 1
 #define LOCKS_DTYPE_Q4 2
+#define LOCKS_DTYPE_BF16_PACKED 3
 
 /* Bytes of one page-head of a LOCKS_DTYPE_Q4 summary at rank r and page size
  * P (head_dim 128): 64r basis + 128 centroid + P r coefficients + 4(2r+1)
@@ -127,6 +128,13 @@ typedef struct locks_cache {
  *   dtype    LOCKS_DTYPE_BF16 for everything that reads summaries;
  *            LOCKS_DTYPE_F32 is accepted by locks_build_summaries only (a
  *            full-precision copy for validation);
+ *            LOCKS_DTYPE_BF16_PACKED: the same bf16 values in one block per
+ *            page-head, basis_t pointing to [pages_total][num_kv_heads]
+ *            [rank * head_dim + page_size * rank]: the rank basis rows (as
+ *            basis_t above) followed by the page_size x rank coefficients
+ *            (as coeffs above); coeffs is unused.  The scan fetches a page's
+ *            blocks for several KV heads with one copy instead of two, which
+ *            makes it the faster bf16 layout;
  *            LOCKS_DTYPE_Q4: the quantised, centred format of the explainer's
  *            §2 "Kernmechanisme", Kwantisatie (int4 basis, int8 coefficients and centroid),
  *            rank 2..8.  Then basis_t points to one block of

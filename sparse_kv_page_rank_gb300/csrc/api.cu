@@ -73,13 +73,14 @@ locks_status_t check_params(const locks_cache_t* c, const locks_params_t* p) {
 
 locks_status_t check_summary(const locks_summary_t* s, bool for_scan) {
   if (!s || !s->basis_t) return LOCKS_ERR_INVALID_ARG;
-  const bool q4 = s->dtype == LOCKS_DTYPE_Q4;  // one packed array; coeffs unused
-  if (!q4 && !s->coeffs) return LOCKS_ERR_INVALID_ARG;
+  const bool q4 = s->dtype == LOCKS_DTYPE_Q4;
+  const bool one = q4 || s->dtype == LOCKS_DTYPE_BF16_PACKED;  // one array of blocks; coeffs unused
+  if (!one && !s->coeffs) return LOCKS_ERR_INVALID_ARG;
   if (s->rank < 2 || s->rank > 16 || (s->rank & 1)) return LOCKS_ERR_UNSUPPORTED;
-  if (s->dtype != LOCKS_DTYPE_BF16 && s->dtype != LOCKS_DTYPE_F32 && !q4) return LOCKS_ERR_INVALID_ARG;
+  if (s->dtype != LOCKS_DTYPE_BF16 && s->dtype != LOCKS_DTYPE_F32 && !one) return LOCKS_ERR_INVALID_ARG;
   if (q4 && s->rank > 8) return LOCKS_ERR_UNSUPPORTED;
   if (for_scan && s->dtype == LOCKS_DTYPE_F32) return LOCKS_ERR_UNSUPPORTED;
-  if ((reinterpret_cast<uintptr_t>(s->basis_t) | (q4 ? 0 : reinterpret_cast<uintptr_t>(s->coeffs))) & 15)
+  if ((reinterpret_cast<uintptr_t>(s->basis_t) | (one ? 0 : reinterpret_cast<uintptr_t>(s->coeffs))) & 15)
     return LOCKS_ERR_INVALID_ARG;
   return LOCKS_OK;
 }
@@ -274,6 +275,7 @@ locks_status_t run_select(const locks_cache_t* c, const locks_summary_t* s, cons
   sa.n_chunks = pl.n_scan;
   sa.scale_log2 = scale_of(p) * kLog2e;
   sa.q4 = s->dtype == LOCKS_DTYPE_Q4 ? 1 : 0;
+  sa.packed = s->dtype == LOCKS_DTYPE_BF16_PACKED ? 1 : 0;
   sa.page_size = c->page_size;
   sa.heads_per_block = pl.scan_hg;
   sa.slots = sa.slot_bytes = sa.basis_bytes = sa.coef_bytes = 0;  // set by the launcher

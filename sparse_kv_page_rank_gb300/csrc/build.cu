@@ -459,8 +459,10 @@ __global__ void __launch_bounds__(kBT) build_kernel(const BuildArgs a) {
     for (int e = tid; e < r * kHeadDim; e += kBT) bo[e] = s.V[(e / kHeadDim) * kVS + e % kHeadDim];
     for (int e = tid; e < P * r; e += kBT) co[e] = s.Y[(e / r) * kXS + e % r];
   } else {
-    uint16_t* bo = reinterpret_cast<uint16_t*>(a.basis_t) + ph * (size_t)r * kHeadDim;
-    uint16_t* co = reinterpret_cast<uint16_t*>(a.coeffs) + ph * (size_t)P * r;
+    // bf16: two arrays, or one block per page-head (basis rows, then coefficients)
+    const bool packed = a.format == LOCKS_DTYPE_BF16_PACKED;
+    uint16_t* bo = reinterpret_cast<uint16_t*>(a.basis_t) + ph * (size_t)r * (packed ? kHeadDim + P : kHeadDim);
+    uint16_t* co = packed ? bo + r * kHeadDim : reinterpret_cast<uint16_t*>(a.coeffs) + ph * (size_t)P * r;
     for (int e = tid; e < r * kHeadDim; e += kBT)
       bo[e] = __bfloat16_as_ushort(__float2bfloat16_rn(s.V[(e / kHeadDim) * kVS + e % kHeadDim]));
     for (int e = tid; e < P * r; e += kBT)

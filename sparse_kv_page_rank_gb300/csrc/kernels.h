@@ -23,6 +23,7 @@ struct ScanArgs {
   int chunk_pages, n_chunks;
   float scale_log2;            // scale * log2(e)
   int q4;                      // 1: basis_t holds LOCKS_DTYPE_Q4 blocks (coeffs unused)
+  int packed;                  // 1: basis_t holds LOCKS_DTYPE_BF16_PACKED blocks (coeffs unused)
   int page_size;               // P: 64 or 16
   int heads_per_block;         // HG: KV heads one CTA scans together (a power of two dividing Hkv, <= 4)
   // set by the launcher: ring of `slots` slots, one page of the head block each

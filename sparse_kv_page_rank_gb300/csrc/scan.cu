@@ -75,17 +75,18 @@ constexpr int kStagePend = kScanWarps * kMuBatch * 16 * 4;   // base-2 LSE per h
 
 // Layout of one slot (a page of a head block) and the ring for these shapes.
 struct SlotLayout {
-  int basis_bytes;  // per page-head: r rows of 256 B (quantised: the whole packed block)
-  int coef_bytes;   // per page-head: P x r bf16 (quantised: 0)
+  int basis_bytes;  // per page-head: r rows of 256 B (quantised or packed bf16: the whole block)
+  int coef_bytes;   // per page-head: P x r bf16 (quantised or packed bf16: 0, inside the block)
   int slot_bytes;   // HG page-heads
   int slots;
   int smem;         // dynamic shared memory of the kernel
 };
 
-SlotLayout slot_layout(int rank, int page_size, int hg, bool q4) {
+SlotLayout slot_layout(int rank, int page_size, int hg, bool q4, bool packed) {
   SlotLayout L;
-  L.basis_bytes = q4 ? LOCKS_Q4_BLOCK_BYTES(rank, page_size) : rank * kHeadDim * 2;
-  L.coef_bytes = q4 ? 0 : page_size * rank * 2;
+  L.basis_bytes = q4 ? LOCKS_Q4_BLOCK_BYTES(rank, page_size)
+                     : rank * kHeadDim * 2 + (packed ? page_size * rank * 2 : 0);
+  L.coef_bytes = q4 || packed ? 0 : page_size * rank * 2;
   L.slot_bytes = hg * (L.basis_bytes + L.coef_bytes);
   const int groups = kScanWarps / hg;
   int s = (q4 ? kRingBytesQ4 : kRingBytes) / L.slot_bytes;
@@ -468,7 +469,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(const ScanArgs a)
           mbar_arrive_expect_tx(&full_bar[lane], bb + cb);
           bulk_load_hint(slot, reinterpret_cast<const uint8_t*>(a.basis_t) + ph * a.basis_bytes, bb, &full_bar[lane],
                          once);
-          if (!Q4)
+          if (!Q4 && cb)  // the two-array bf16 layout: the coefficients separately
             bulk_load_hint(slot + bb, reinterpret_cast<const uint8_t*>(a.coeffs) + ph * a.coef_bytes, cb,
                            &full_bar[lane], once);
         } else {
@@ -503,8 +504,10 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(const ScanArgs a)
     }
     // this head's basis (or packed block) and coefficients in slot s
     auto head_basis = [&](int s) -> uint32_t { return ring + s * slot_bytes + hw * a.basis_bytes; };
+    // (packed bf16 blocks: the coefficients follow the basis rows)
     auto head_coef = [&](int s) -> uint32_t {
-      return ring + s * slot_bytes + HG * a.basis_bytes + hw * a.coef_bytes;
+      return a.packed ? head_basis(s) + (uint32_t)(r * kHeadDim * 2)
+                      : ring + s * slot_bytes + HG * a.basis_bytes + hw * a.coef_bytes;
     };
     unsigned long long cyc_wait = 0, cyc_comp = 0;
     // quantised format: this warp's pending pages (centroid codes, centroid
@@ -648,7 +651,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) scan_kernel(const ScanArgs a)
 template <bool G16, bool R16, bool GRP2, bool Q4, int P>
 cudaError_t launch_one(const ScanArgs& a0, cudaStream_t s, bool pdl) {
   ScanArgs a = a0;
-  const SlotLayout L = slot_layout(a.rank, P, a.heads_per_block, Q4);
+  const SlotLayout L = slot_layout(a.rank, P, a.heads_per_block, Q4, a.packed != 0);
   a.slots = L.slots;
   a.slot_bytes = L.slot_bytes;
   a.basis_bytes = L.basis_bytes;

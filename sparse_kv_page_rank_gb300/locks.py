@@ -29,6 +29,7 @@ LOCKS_STATIC_WS_BYTES = 8 << 20
 LOCKS_DTYPE_BF16 = 0
 LOCKS_DTYPE_F32 = 1
 LOCKS_DTYPE_Q4 = 2
+LOCKS_DTYPE_BF16_PACKED = 3
 LOCKS_FLAG_UNFUSED = 0x1
 LOCKS_FLAG_FUSED = 0x2
 

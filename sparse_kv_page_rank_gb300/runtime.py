@@ -17,9 +17,12 @@ class LocksRuntime:
 
     k_pool, v_pool: bf16 [pages_total][Hkv][P][128] with P = 64 or 16;
     block_table int32 [B][max_pages]; seq_lens, n_summarized int32 [B].
-    Summaries are allocated here: bf16 [pages_total][Hkv][rank][128] and
-    [..][P][rank], or, with ``quantized``, one packed LOCKS_DTYPE_Q4 block per
-    page-head (uint8 [pages_total][Hkv][q4_page_head_bytes(rank, P)]).
+    Summaries are allocated here.  bf16: one LOCKS_DTYPE_BF16_PACKED block per
+    page-head (basis rows, then coefficients), with ``basis_t`` [pages_total]
+    [Hkv][rank][128] and ``coeffs`` [..][P][rank] as views into it; with
+    ``split`` two separate LOCKS_DTYPE_BF16 arrays of those shapes instead.
+    With ``quantized``: one LOCKS_DTYPE_Q4 block per page-head (uint8
+    [pages_total][Hkv][q4_page_head_bytes(rank, P)]).
     ``form``: "auto" (the library's choice: three kernels), or "unfused" /
     "fused" for LOCKS_FLAG_UNFUSED / LOCKS_FLAG_FUSED (the decode step as three
     kernels, or as two wherever the size limits allow).
@@ -27,7 +30,8 @@ class LocksRuntime:
 
     def __init__(self, k_pool: torch.Tensor, v_pool: torch.Tensor, block_table: torch.Tensor,
                  seq_lens: torch.Tensor, n_summarized: torch.Tensor, num_q_heads: int, rank: int,
-                 budget_tokens: int, scale: float = 0.0, quantized: bool = False, form: str = "auto"):
+                 budget_tokens: int, scale: float = 0.0, quantized: bool = False, form: str = "auto",
+                 split: bool = False):
         assert k_pool.dtype == torch.bfloat16 and v_pool.dtype == torch.bfloat16
         assert block_table.dtype == torch.int32 and seq_lens.dtype == torch.int32
         self.device = k_pool.device
@@ -43,12 +47,17 @@ class LocksRuntime:
             self.basis_t = torch.zeros((pt, hkv, L.q4_page_head_bytes(rank, P)), dtype=torch.uint8,
                                        device=self.device)
             self.coeffs = None
-        else:
+            self.summary = L.make_summary(self.basis_t, None, rank, L.LOCKS_DTYPE_Q4)
+        elif split:
             self.basis_t = torch.zeros((pt, hkv, rank, d), dtype=torch.bfloat16, device=self.device)
             self.coeffs = torch.zeros((pt, hkv, P, rank), dtype=torch.bfloat16, device=self.device)
+            self.summary = L.make_summary(self.basis_t, self.coeffs, rank, L.LOCKS_DTYPE_BF16)
+        else:
+            self.blocks = torch.zeros((pt, hkv, rank * d + P * rank), dtype=torch.bfloat16, device=self.device)
+            self.basis_t = self.blocks[:, :, :rank * d].unflatten(-1, (rank, d))
+            self.coeffs = self.blocks[:, :, rank * d:].unflatten(-1, (P, rank))
+            self.summary = L.make_summary(self.blocks, None, rank, L.LOCKS_DTYPE_BF16_PACKED)
         self.cache = L.make_cache(k_pool, v_pool, block_table, seq_lens, self.n_summarized)
-        self.summary = L.make_summary(self.basis_t, self.coeffs, rank,
-                                      L.LOCKS_DTYPE_Q4 if quantized else L.LOCKS_DTYPE_BF16)
         flags = {"auto": 0, "unfused": L.LOCKS_FLAG_UNFUSED, "fused": L.LOCKS_FLAG_FUSED}[form]
         self.params = L.make_params(num_q_heads, budget_tokens, scale, flags)
         self.k_max = min(budget_tokens // P, block_table.shape[1])

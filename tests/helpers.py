@@ -144,7 +144,8 @@ def torch_bf16_to_u16(t):
     return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def make_runtime(case, rank: int, budget_tokens: int, n_summarized=None, device="cuda", quantized=False):
+def make_runtime(case, rank: int, budget_tokens: int, n_summarized=None, device="cuda", quantized=False,
+                 split=False):
     import torch
     from sparse_kv_page_rank_gb300.runtime import LocksRuntime
     if n_summarized is None:
@@ -153,7 +154,7 @@ def make_runtime(case, rank: int, budget_tokens: int, n_summarized=None, device=
                       torch.from_numpy(case.block_table).to(device),
                       torch.from_numpy(case.seq_lens).to(device),
                       torch.tensor(np.asarray(n_summarized, dtype=np.int32)).to(device),
-                      case.num_q_heads, rank, budget_tokens, quantized=quantized)
+                      case.num_q_heads, rank, budget_tokens, quantized=quantized, split=split)
     q = to_torch_bf16(case.q, device)
     return rt, q
 

@@ -121,6 +121,19 @@ def test_bad_summary_rejected_before_launch(lib, rank, dtype, status):
     assert e.value.status == status
 
 
+def test_packed_summary_needs_no_coefficient_array(lib):
+    """LOCKS_DTYPE_BF16_PACKED (one block per page-head) passes the summary
+    checks with coeffs NULL and stops only at the missing workspace; the
+    two-array layout without coeffs is rejected."""
+    p = L.make_params(8, 512)
+    for dtype, status in ((L.LOCKS_DTYPE_BF16_PACKED, L.LOCKS_ERR_WORKSPACE),
+                          (L.LOCKS_DTYPE_BF16, L.LOCKS_ERR_INVALID_ARG)):
+        with pytest.raises(L.LocksError) as e:
+            L.locks_select(_cache(), L.make_summary(0x10000, None, 8, dtype), p, 0x9000, 0xA000, 0xB000, None,
+                           None, 0, 0)
+        assert e.value.status == status, dtype
+
+
 def test_workspace_checks_before_launch(lib):
     s = L.locks_summary_t(0x10000, 0x20000, 8, 0)
     p = L.make_params(8, 512)

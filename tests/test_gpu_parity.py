@@ -11,7 +11,9 @@ Tolerances (fixed up front):
     error e = ||K - C V^T||_F / ||K||_F.
 Inputs: seeded synthetic page-local low-rank caches (synth), with ragged
 lengths, partial tail pages, unsummarised full pages, several scan / top-k
-chunks, G in {1, 2, 4, 16} and r in {2, 4, 8, 16}.
+chunks, G in {1, 2, 4, 16} and r in {2, 4, 8, 16}.  bf16 summaries are in the
+runtime's packed layout (LOCKS_DTYPE_BF16_PACKED) unless a case asks for the
+two-array layout (LOCKS_DTYPE_BF16).
 """
 
 import math
@@ -45,12 +47,12 @@ def _upload_summaries(rt, basis_t, coeffs):
     rt.set_summaries(to_torch_bf16(basis_t, rt.device), to_torch_bf16(coeffs, rt.device))
 
 
-def _run_case(case, r, budget, nsum=None, check_dense=True):
+def _run_case(case, r, budget, nsum=None, check_dense=True, split=False):
     """Identical-summary parity of select, decode_step and dense decode."""
     if nsum is None:
         nsum = [case.n_full_pages(b) for b in range(case.batch)]
     basis_t, coeffs = oracle_summaries_bf16(case, r)
-    rt, q = make_runtime(case, r, budget, nsum)
+    rt, q = make_runtime(case, r, budget, nsum, split=split)
     _upload_summaries(rt, basis_t, coeffs)
     page_lse = torch.full((case.batch, case.num_q_heads, case.max_pages), float("nan"), device="cuda")
     rt.select(q, page_lse)
@@ -104,11 +106,12 @@ def _run_case(case, r, budget, nsum=None, check_dense=True):
     return rt, q, ref, worst_lse
 
 
+@pytest.mark.parametrize("split", [False, True])
 @pytest.mark.parametrize("G,Hkv,r", [(4, 2, 8), (1, 1, 8), (2, 3, 4), (16, 2, 8), (4, 2, 16), (8, 1, 2)])
-def test_select_and_step_ragged(G, Hkv, r):
+def test_select_and_step_ragged(G, Hkv, r, split):
     case = make_case(2, G * Hkv, Hkv, [64 * 41 + 17, 64 * 37], true_rank=(2, 12), n_carriers=2,
                      seed=100 + G + r, spare_pages=3)
-    _run_case(case, r, budget=64 * 6)
+    _run_case(case, r, budget=64 * 6, split=split)
 
 
 def test_unsummarised_full_pages_join_the_tail():
@@ -408,3 +411,35 @@ def test_decode_step_with_host_query_and_output():
     assert rt.device_error() == 0
     assert torch.equal(out_host.view(torch.int16), out_dev.cpu().view(torch.int16))
     assert torch.equal(lse_host, lse_dev.cpu())
+
+
+@pytest.mark.parametrize("P", [64, 16])
+def test_packed_layout_holds_the_two_array_values(P):
+    """LOCKS_DTYPE_BF16_PACKED: the builder writes bit-for-bit the values of
+    the two-array bf16 layout, basis rows then coefficients in one block per
+    page-head, and the scan gives bit-identical page LSEs from either."""
+    from sparse_kv_page_rank_gb300 import locks as L
+    r = 8
+    case = make_case(2, 8, 2, [P * 30 + 3, P * 22], true_rank=(2, 10), n_carriers=2, seed=61, page_size=P)
+    dev = "cuda"
+    split, q = make_runtime(case, r, P * 6, split=True)
+    packed, _ = make_runtime(case, r, P * 6)
+    assert packed.summary.dtype == L.LOCKS_DTYPE_BF16_PACKED and split.summary.dtype == L.LOCKS_DTYPE_BF16
+    pages = torch.from_numpy(np.concatenate([case.block_table[b, :case.n_full_pages(b)]
+                                             for b in range(case.batch)])).to(dev)
+    split.build_summaries(pages)
+    packed.build_summaries(pages)
+    torch.cuda.synchronize()
+    blocks = packed.blocks.view(torch.int16)
+    pt, hkv = blocks.shape[:2]
+    assert torch.equal(blocks[:, :, :r * 128], split.basis_t.view(torch.int16).reshape(pt, hkv, -1))
+    assert torch.equal(blocks[:, :, r * 128:], split.coeffs.view(torch.int16).reshape(pt, hkv, -1))
+    pls = []
+    for rt in (split, packed):
+        pl = torch.full((case.batch, case.num_q_heads, case.max_pages), float("nan"), device=dev)
+        rt.select(q, pl)
+        torch.cuda.synchronize()
+        assert rt.device_error() == 0
+        pls.append(pl)
+    assert torch.equal(torch.nan_to_num(pls[0], nan=7.0), torch.nan_to_num(pls[1], nan=7.0))
+    assert torch.equal(split.sel_pages, packed.sel_pages) and torch.equal(split.sel_count, packed.sel_count)
