@@ -651,6 +651,26 @@ def run_gpu(args):
                  "timing": {"l2": f"rotating {r1['R']} independent copies of cache + summaries "
                                   f"({r1['R'] * r1['per_copy'] / 1e9:.2f} GB > 129 MB L2)"}}
 
+    # the other named workloads at their stated shapes (step, dense, scan,
+    # recall, clocks), and the growing-cache loop at its full 1024 steps
+    workloads = None
+    if args.config == "llama128k" and args.page_size == P and not args.rank and not args.no_workloads \
+            and world == 1:
+        workloads = {}
+        for key, name, rk in (("sweep_r2", "sweep", 2), ("sweep_r4", "sweep", 4), ("sweep_r8", "sweep", 8),
+                              ("tiny", "tiny", None), ("growing", "growing", None)):
+            rw = _gpu_workload(args, name, K, W, world, dev, rank_override=rk, full=False, q4=False)
+            ew = rw["step_bytes"]["total"] / (rw["step_ms"] * 1e-3) / 1e9
+            workloads[key] = {
+                "value": rw["step_ms"] * 1e3, "unit": "us", "config": rw["config"],
+                "step_us_over_replays": rw["step_pct"], "dense_us": rw["dense_ms"] * 1e3,
+                "speedup_vs_dense": rw["dense_ms"] / rw["step_ms"], "effective_gbs": ew, "step_frac_of_hbm": ew / peak,
+                "kv_bytes_ratio": rw["dense_bytes"] / rw["step_bytes"]["total"], "residency": residency(rw["r"], rw["P"]),
+                "mass_recall": rw["mass_recall"], "exact_lse_selection_recall": rw["exact_lse_selection_recall"],
+                "carrier_retention": rw["carrier_retention"], "roofline": _roofline(rw, peak, peak_kind),
+                "gpu_launches": rw["launches"] * K, "clocks": rw["clocks"]}
+        workloads["growing_loop"] = _growing_loop(args, dev, 16)
+
     # batched throughput at 256K context on device-drawn page-local caches
     batched = None
     if args.config == "llama128k" and args.page_size == P and not args.rank and not args.no_batched and world == 1:
@@ -713,6 +733,7 @@ def run_gpu(args):
         "q4": res["q4"],
         "ctx1m": ctx1m,
         "batched_256k": batched,
+        "workloads": workloads,
         "gpu_launches": res["launches"] * K,
         "clocks": res["clocks"],
     }
@@ -723,6 +744,16 @@ def run_gpu(args):
 
 
 def run_growing(args):
+    import torch
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    from sparse_kv_page_rank_gb300.build_lib import build
+    build()
+    print(json.dumps(_growing_loop(args, dev, max(3, args.growing_segments))))
+
+
+def _growing_loop(args, dev, segments) -> dict:
     """The growing-cache loop of the batch-32 8K workload (32 q / 8 KV heads,
     rank 4, budget 1024): each decode step appends one token to every
     sequence, and whenever the sequences' last pages fill, the builder
@@ -733,14 +764,9 @@ def run_growing(args):
     second against the rate at which pages fill."""
     import torch
 
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
-    from sparse_kv_page_rank_gb300.build_lib import build
-    build()
     from sparse_kv_page_rank_gb300.growing import GrowingLoop
     from sparse_kv_page_rank_gb300.runtime import LocksRuntime
 
-    segments = max(3, args.growing_segments)
     start = 8192
     case, cfg = make_config_case("growing", context=start + P * segments)
     r, budget = cfg["rank"], cfg["budget_tokens"]
@@ -766,7 +792,7 @@ def run_growing(args):
     loop.run(segments, build=True)  # warm-up; also leaves every filling page summarised once
     loop.reset()
     reps = 3
-    clocks = ClockSampler(0)
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
     clocks.start()
     time.sleep(0.3)
     with_b, without_b = [], []
@@ -804,7 +830,9 @@ def run_growing(args):
                    "graph": f"one CUDA graph per {P}-step segment; events on the main and side streams"},
         "clocks": clk,
     }
-    print(json.dumps(line))
+    del loop, rt, k, v
+    torch.cuda.empty_cache()
+    return line
 
 
 def _batched_256k(args, dev, K, W, batches) -> dict:
@@ -942,6 +970,8 @@ def main():
     ap.add_argument("--rank", type=int, default=0, help="summary rank (0 = the workload's own)")
     ap.add_argument("--no-ctx1m", action="store_true", help="skip the 1M-context sub-measurement")
     ap.add_argument("--no-batched", action="store_true", help="skip the batched 256K sub-measurement")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other workloads' sub-measurements (sweep, tiny, growing, growing loop)")
     args = ap.parse_args()
     if args.batch_sweep:
         run_batch_sweep(args)
