@@ -40,7 +40,7 @@ struct Plan {
   bool fused = false;     // decode step as scan + one attention kernel that selects the pages itself
   int fused_cluster = 1;
   size_t off_err = 0, off_cnt_tk = 0, off_cnt_att = 0, off_shat = 0, off_part = 0, off_ckey = 0,
-         off_cidx = 0, off_sel = 0, off_selcnt = 0, off_pml = 0, off_po = 0, total = 0;
+         off_cidx = 0, off_sel = 0, off_selcnt = 0, off_selphys = 0, off_pml = 0, off_po = 0, total = 0;
 };
 
 locks_status_t check_cache(const locks_cache_t* c, bool need_kv) {
@@ -198,6 +198,7 @@ Plan make_plan(const locks_cache_t* c, const locks_params_t* p) {
   pl.off_cidx = take(sizeof(int32_t) * BH * pl.n_tk * std::max(pl.k_max, 1));
   pl.off_sel = take(sizeof(int32_t) * BH * std::max(pl.k_max, 1));
   pl.off_selcnt = take(sizeof(int32_t) * BH);
+  pl.off_selphys = take(sizeof(int32_t) * BH * std::max(pl.k_max, 1));
   pl.off_pml = take(sizeof(float2) * BH * pl.dense_nc * pl.G);
   pl.off_po = take(sizeof(float) * BH * pl.dense_nc * pl.G * kHeadDim);
   pl.total = off;
@@ -251,9 +252,11 @@ bool encode_pool(CUtensorMap* m, const void* pool, const locks_cache_t* c) {
 
 locks_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? LOCKS_OK : LOCKS_ERR_CUDA; }
 
+// in_step: the top-k inside locks_decode_step, whose attention kernel reads
+// the physical pages it writes (one-chunk problems)
 locks_status_t run_select(const locks_cache_t* c, const locks_summary_t* s, const locks_params_t* p,
                           const Plan& pl, const void* q, int32_t* sel, int32_t* selcnt, float* page_lse,
-                          void* ws, cudaStream_t st) {
+                          void* ws, cudaStream_t st, bool in_step = false) {
   ScanArgs sa;
   sa.basis_t = static_cast<const uint16_t*>(s->basis_t);
   sa.coeffs = static_cast<const uint16_t*>(s->coeffs);
@@ -294,6 +297,8 @@ locks_status_t run_select(const locks_cache_t* c, const locks_summary_t* s, cons
   ta.counters = at<unsigned>(ws, pl.off_cnt_tk);
   ta.sel_pages = sel;
   ta.sel_count = selcnt;
+  ta.block_table = c->block_table;
+  ta.sel_phys = in_step && pl.n_tk == 1 ? at<int32_t>(ws, pl.off_selphys) : nullptr;
   ta.err = sa.err;
   ta.batch = c->batch;
   ta.num_kv_heads = c->num_kv_heads;
@@ -322,6 +327,10 @@ locks_status_t run_attend(const locks_cache_t* c, const locks_params_t* p, const
   a.n_summarized = c->n_summarized;
   a.sel_pages = sel;
   a.sel_count = selcnt;
+  // inside the decode step the top-k also wrote the selected pages' physical
+  // ids (one-chunk problems), which saves the block-table lookup
+  a.sel_phys = (mode == kAttendSparse && inputs_early && pl.n_tk == 1 && ws) ? at<int32_t>(ws, pl.off_selphys)
+                                                                             : nullptr;
   a.out = static_cast<uint16_t*>(out);
   a.lse = lse;
   a.page_lse = page_lse;
@@ -507,7 +516,7 @@ locks_status_t locks_decode_step(const locks_cache_t* cache, const locks_summary
     if ((st = run_select(cache, summary, params, pl, q, nullptr, nullptr, nullptr, ws, s)) != LOCKS_OK) return st;
     return run_attend(cache, params, pl, q, sel, cnt, out, lse, nullptr, ws, kAttendFused, s, true);
   }
-  if ((st = run_select(cache, summary, params, pl, q, sel, cnt, nullptr, ws, s)) != LOCKS_OK) return st;
+  if ((st = run_select(cache, summary, params, pl, q, sel, cnt, nullptr, ws, s, true)) != LOCKS_OK) return st;
   return run_attend(cache, params, pl, q, sel, cnt, out, lse, nullptr, ws, kAttendSparse, s, true);
 }
 

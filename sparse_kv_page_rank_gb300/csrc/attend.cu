@@ -67,10 +67,15 @@ template <int MODE, int P>
 __device__ __forceinline__ Item get_item(const AttendArgs& a, int i, int b, int bh, int L, int ns,
                                          int cnt) {
   Item it;
-  int lp;
+  int lp, phys = -1;
+  bool known = false;  // physical page already given with the selection
   if (MODE == kAttendSparse) {
     if (i < cnt) {
       lp = a.sel_pages[(size_t)bh * a.k_max + i];
+      if (a.sel_phys) {  // loaded alongside, not after, the logical page
+        phys = a.sel_phys[(size_t)bh * a.k_max + i];
+        known = true;
+      }
       if (lp < 0 || lp >= ns) {
         set_error(a.err, LOCKS_DEVERR_SEL_PAGE);
         lp = -1;
@@ -85,7 +90,7 @@ __device__ __forceinline__ Item get_item(const AttendArgs& a, int i, int b, int 
   it.phys = 0;
   it.len = 0;
   if (lp >= 0) {
-    int phys = a.block_table[(size_t)b * a.max_pages + lp];
+    if (!known) phys = a.block_table[(size_t)b * a.max_pages + lp];
     if (phys < 0 || phys >= a.pages_total) {
       set_error(a.err, LOCKS_DEVERR_BLOCK_TABLE);
       it.lp = -1;

@@ -42,6 +42,8 @@ struct TopkArgs {
   unsigned* counters;   // ws: [B*Hkv]
   int32_t* sel_pages;   // [B*Hkv][k_max]
   int32_t* sel_count;   // [B*Hkv]
+  const int32_t* block_table;  // read before the grid dependency wait when sel_phys is set
+  int32_t* sel_phys;    // ws: [B*Hkv][k_max] physical page of each selected page (one-chunk problems), or null
   int* err;
   int batch, num_kv_heads, group, max_pages, k_max;
   int chunk_pages, n_chunks;
@@ -58,6 +60,7 @@ struct AttendArgs {
   const int32_t* n_summarized;
   const int32_t* sel_pages;   // sparse mode only
   const int32_t* sel_count;   // sparse mode only
+  const int32_t* sel_phys;    // sparse mode inside the decode step: physical pages of sel_pages, or null
   uint16_t* out;              // bf16 [B][Hq][d]
   float* lse;                 // optional [B][Hq]
   float* page_lse;            // page_lse mode: [B][Hq][max_pages]

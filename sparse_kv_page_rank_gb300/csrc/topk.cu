@@ -420,6 +420,17 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkArgs a)
   const int G = GT ? GT : a.group;
 
   trace_mark(a.err, kTrTopkEnter, true);
+  const int j0 = chunk * a.chunk_pages;
+  if (!MULTI && a.sel_phys) {
+    // inside the decode step: the block table is an input of the step, so
+    // this problem's row loads while the scan is still running (idx is free
+    // in a one-chunk problem; thread t keeps the entries of its own pages)
+#pragma unroll
+    for (int p = 0; p < IPT; ++p) {
+      const int j = j0 + tid + kTopkThreads * p;
+      if (j < a.max_pages) idx[j - j0] = __ldg(a.block_table + (size_t)b * a.max_pages + j);
+    }
+  }
   pdl_wait();
   trace_mark(a.err, kTrTopkWait, true);
   // the attention kernel that follows may start its prologue now; it waits
@@ -442,7 +453,6 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkArgs a)
     }
   }
   // pages j0 + tid + kTopkThreads * p: a warp reads consecutive rows
-  const int j0 = chunk * a.chunk_pages;
   float sv[IPT][GMAX];
   {
     const float* sbase = a.shat + (size_t)bh * a.max_pages * G;
@@ -476,11 +486,15 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkArgs a)
   ns = ns < 0 ? 0 : (ns > cap ? cap : ns);
   const int k = ns < a.k_max ? ns : a.k_max;
   int32_t* sel = a.sel_pages + (size_t)bh * a.k_max;
+  int32_t* sphys = (!MULTI && a.sel_phys) ? a.sel_phys + (size_t)bh * a.k_max : nullptr;
 
   if (ns <= a.k_max) {
     // every summarised page is selected
     if (chunk == 0) {
-      for (int i = tid; i < ns; i += kTopkThreads) sel[i] = i;
+      for (int i = tid; i < ns; i += kTopkThreads) {
+        sel[i] = i;
+        if (sphys) sphys[i] = idx[i];  // written by this thread above
+      }
       if (tid == 0) a.sel_count[bh] = ns;
     }
     trace_mark(a.err, kTrTopkExit, false);
@@ -542,7 +556,10 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkArgs a)
 
   const int kloc = k < nloc ? k : nloc;
   if constexpr (!MULTI) {
-    reg_select<IPT>(kr, keys, nloc, kloc, sh, fsh, [&](int pos, int i) { sel[pos] = j0 + i; }, a.err);
+    reg_select<IPT>(kr, keys, nloc, kloc, sh, fsh, [&](int pos, int i) {
+      sel[pos] = j0 + i;
+      if (sphys) sphys[pos] = idx[i];
+    }, a.err);
     if (tid == 0) a.sel_count[bh] = kloc;
     trace_mark(a.err, kTrTopkSelected, false);
     trace_mark(a.err, kTrTopkExit, false);
