@@ -15,10 +15,13 @@
 // page of the block per slot.  The summaries of a physical page are laid out
 // head after head, so a page's bases for all HG heads are one contiguous
 // range and so are its coefficients: one producer warp fills a slot with two
-// TMA bulk copies (one for the quantised format) per page and head block.
+// TMA bulk copies per page and head block, or one for the quantised format
+// and for packed bf16 blocks (basis and coefficients of a page-head together).
 // The copy count, not the bytes, limits a TMA read of small pieces (about
 // 40 ns per copy per SM measured on GB300, whatever the size up to ~1 KiB), so
 // covering HG page-heads per copy is what lets the scan stream at HBM speed.
+// The loads carry an L2 evict-first policy: every summary is read once per
+// step, and the s_hat rows written here should stay in L2 for the top-k.
 // Each of the producer's lanes owns a slot, waits for it to be released and
 // refills it, completing on the slot's "full" mbarrier.  Sixteen consumer
 // warps only compute: warp w serves head w mod HG of the block and every
