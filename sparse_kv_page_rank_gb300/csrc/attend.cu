@@ -20,12 +20,16 @@
 // by ldmatrix.trans.
 //
 // Merging partial softmax states (max m, sum l, O): the four warps of a CTA
-// in shared memory; the CTAs of a cluster through distributed shared memory
-// (after a cluster barrier, CTA rank c reads every CTA's state for output
-// columns [c*128/CS, (c+1)*128/CS)); with NC > 1 the clusters of a problem
-// write their partial to the workspace and the last cluster to finish (atomic
-// ticket, no waiting) merges them, again one column slice per CTA.  The
-// result is o (bf16) and lse (natural log).
+// in shared memory; then the CTAs of a cluster through distributed shared
+// memory, CTA rank c owning output columns [c*128/CS, (c+1)*128/CS).  With a
+// page list (one cluster per problem) each CTA pushes its state for those
+// columns into their owner's shared memory and arrives on the owner's barrier,
+// and each owner merges what it received (nobody reads remote memory, so no
+// CTA waits for the others before it exits).  For every page (dense mode)
+// each CTA reads the cluster's states after a cluster barrier; with NC > 1
+// the clusters of a problem write their partial to the workspace and the last
+// cluster to finish (atomic ticket, no waiting) merges them, again one column
+// slice per CTA.  The result is o (bf16) and lse (natural log).
 //
 // 16-token pages (the explainer's §2 "Kernmechanisme" page size): a tile is
 // four pages, loaded as four 16-row boxes into the rows 16w..16w+15 that warp

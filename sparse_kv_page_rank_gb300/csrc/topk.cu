@@ -14,11 +14,18 @@
 //   * grid (n_chunks, B*Hkv); CTA (chunk, bh) owns pages
 //     [chunk*chunk_pages, (chunk+1)*chunk_pages) of problem bh;
 //   * Z_h from the scan's per-CTA (max, sum) partials (warp per head);
-//   * sigma_j for the chunk -> 32-bit order-preserving keys in shared memory;
-//   * MSB-first 8-bit radix select finds the k-th largest key T and how many
-//     keys equal to T to take; an ordered block scan then keeps every key > T
-//     and the first such keys == T in page order, so the output is already
-//     sorted ascending and ties go to lower pages;
+//   * sigma_j for the chunk -> 32-bit order-preserving keys, held in
+//     registers (a thread's pages) and in shared memory;
+//   * one 2048-bin histogram of the top 11 bits in which the keys differ
+//     finds the bin holding the k-th largest key; the keys of that bin are
+//     ranked against each other (key descending, page ascending) and the
+//     chosen pages are numbered in page order with warp ballots, so the output
+//     is already sorted ascending and ties go to lower pages.  A boundary bin
+//     of more than 512 keys (many equal keys) falls back to an MSB-first 8-bit
+//     radix select over the differing bits and an ordered block scan;
+//   * inside the decode step a one-chunk problem also writes each chosen
+//     page's physical id, from a block-table row it loads before its
+//     grid-dependency wait;
 //   * the chunk's candidates go to the workspace; the last CTA of the problem
 //     to finish (atomic ticket, no waiting) reruns the same select over all
 //     candidates, which are laid out in page order, and writes the page list.
