@@ -27,7 +27,6 @@ torch = pytest.importorskip("torch")
 
 pytestmark = pytest.mark.gpu
 
-P = 64
 OUT_ATOL = 1e-2
 LSE_RTOL = 1e-3
 BAND = 1e-4
@@ -45,15 +44,18 @@ def _recon_err(K, V_rows, C):
     return np.linalg.norm(K - C @ V_rows) / np.linalg.norm(K)
 
 
-@pytest.mark.parametrize("form", ["unfused", "fused"])
-def test_growing_loop_matches_oracle(form):
+@pytest.mark.parametrize("form,P", [("unfused", 64), ("fused", 64), ("unfused", 16)])
+def test_growing_loop_matches_oracle(form, P):
+    """A segment is P steps (one page per sequence fills per segment), at
+    64-token pages in both forms of the step and at 16-token pages."""
     from sparse_kv_page_rank_gb300.growing import GrowingLoop
     from sparse_kv_page_rank_gb300.runtime import LocksRuntime
 
-    segments, snap, r, budget = 5, 37, 8, 64 * 8
-    start = np.array([64 * 30, 64 * 45, 64 * 20], dtype=np.int32)
+    segments, r, budget = 5, 8, P * 8
+    snap = 37 * P // 64
+    start = np.array([P * 30, P * 45, P * 20], dtype=np.int32)
     final = start + P * segments
-    case = make_case(3, 8, 2, final.tolist(), true_rank=(4, 12), n_carriers=6, seed=90)
+    case = make_case(3, 8, 2, final.tolist(), true_rank=(4, 12), n_carriers=6, seed=90 + P, page_size=P)
     B, Hkv, G = case.batch, case.num_kv_heads, case.group
     dev = "cuda"
     rt = LocksRuntime(to_torch_bf16(case.k_pool, dev), to_torch_bf16(case.v_pool, dev),
@@ -104,7 +106,8 @@ def test_growing_loop_matches_oracle(form):
     kmax = budget // P
     for s in range(segments):
         sl, ns = snaps["seq_lens"][s], snaps["n_summarized"][s]
-        ref = O.decode_step(case.q, case.k_pool, case.v_pool, case.block_table, sl, ns, ob, oc, Hkv, budget)
+        ref = O.decode_step(case.q, case.k_pool, case.v_pool, case.block_table, sl, ns, ob, oc, Hkv, budget,
+                            page_size=P)
         sel, cnt = snaps["sel_pages"][s], snaps["sel_count"][s]
         for b in range(B):
             for h in range(Hkv):
@@ -116,7 +119,8 @@ def test_growing_loop_matches_oracle(form):
                 ok, detail = cut_band_ok(ref["sigma"][(b, h)], chosen, ref["sel"][(b, h)], k, BAND)
                 assert ok, (s, b, h, detail)
         gsel = {(b, h): sel[b, h, :cnt[b, h]] for b in range(B) for h in range(Hkv)}
-        ro, rl = O.sparse_decode(case.q, case.k_pool, case.v_pool, case.block_table, sl, ns, gsel, Hkv)
+        ro, rl = O.sparse_decode(case.q, case.k_pool, case.v_pool, case.block_table, sl, ns, gsel, Hkv,
+                                 page_size=P)
         go = bf16_to_f32(torch_bf16_to_u16(outs[s])).astype(np.float64)
         gl = snaps["lse"][s].astype(np.float64)
         assert np.isfinite(go).all()
